@@ -1,0 +1,176 @@
+/*
+ * muon.h -- C ABI of libmuon, the Muon optimizer step on whole weight matrices
+ * for one GB300 GPU (sm_103a).
+ *
+ * The method: "Training a 1T-Parameter MoE on EU public infrastructure with
+ * PyTorch and TorchTitan" (PyTorch blog), section "FlexShard: Muon without
+ * communication".  Muon keeps one fp32 state per parameter and orthogonalises
+ * each update with a few Newton-Schulz iterations that act on the whole
+ * matrix; every rank owns complete expert matrices (hidden 6144, expert
+ * hidden 1792 in the model-configuration table), so the step needs no
+ * communication.  The page prints neither the iteration nor its constants;
+ * this library takes them as arguments:
+ *   momentum   buf <- mu*buf + g;  u <- g + mu*buf (Nesterov) or u <- buf
+ *   orient     X = G^T when rows > cols (so X is m x n with m <= n)
+ *   normalise  X <- X / (||X||_F + eps)
+ *   iterate    A = X X^T;  B = b A + c A A;  X <- a X + B X     (steps times)
+ *   update     W <- (1 - lr*wd) W - lr*scale*O
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" are CUDA device (or managed) memory on the
+ *     current device.  The caller owns every buffer; the library keeps no
+ *     per-call state and never frees caller memory.
+ *   - All work is enqueued on `stream` (NULL = the legacy default stream) and
+ *     returns without a host synchronisation.  Argument and launch errors are
+ *     returned at once; device-side failures (a bounded wait that ran out)
+ *     are reported by muon_get_device_status().
+ *   - bf16 means IEEE bfloat16 (16-bit storage); conversions to bf16 round to
+ *     nearest even.  Matrices are row-major, [batch][rows][cols], densely
+ *     packed (matrix i starts at element i*rows*cols).
+ *   - Calls return a muon_status (0 = success, negative = error).
+ */
+#ifndef MUON_H_
+#define MUON_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* A cudaStream_t of the caller (same object); NULL is the legacy default stream. */
+typedef struct CUstream_st *muon_stream_t;
+
+typedef enum {
+  MUON_OK = 0,
+  MUON_ERR_INVALID_ARG = -1,  /* null pointer, negative size, bad coefficient pointer ... */
+  MUON_ERR_UNSUPPORTED = -2,  /* shape or alignment the bf16 tensor-core path does not take */
+  MUON_ERR_CUDA = -3,         /* a CUDA runtime call or kernel launch failed */
+  MUON_ERR_NO_MEMORY = -4,    /* workspace allocation failed or workspace too small */
+  MUON_ERR_TIMEOUT = -5,      /* a device-side bounded wait ran out (kernel returned early) */
+  MUON_ERR_DEVICE = -6        /* a device-side consistency check failed */
+} muon_status;
+
+/* ---------------------------------------------------------------------------
+ * Momentum (FlexShard section: one fp32 state per parameter).
+ *   buf[i] <- fp32(fp32(mu*buf[i]) + g[i])
+ *   u[i]   <- fp32(g[i] + fp32(mu*buf[i]))   if nesterov != 0 (new buf)
+ *   u[i]   <- buf[i]                         otherwise
+ * Each multiply and add is rounded to fp32 separately (no fused multiply-add),
+ * so the result is bit-reproducible.
+ *   grad       device, bf16, numel elements (read)
+ *   momentum   device, fp32, numel elements (read and written in place)
+ *   update_out device, bf16, numel elements (written; u rounded to bf16)
+ *   numel >= 0; numel == 0 is a no-op.  Any alignment is accepted (16-byte
+ *   aligned pointers take the vectorised path).
+ * Errors: MUON_ERR_INVALID_ARG for null pointers with numel > 0 or numel < 0.
+ */
+int muon_momentum_update(const void *grad, float *momentum, void *update_out, int64_t numel,
+                         float mu, int nesterov, muon_stream_t stream);
+
+/* Same arithmetic with an fp32 gradient and an fp32 u (verification mode). */
+int muon_momentum_update_f32(const float *grad, float *momentum, float *update_out, int64_t numel,
+                             float mu, int nesterov, muon_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Batched Newton-Schulz orthogonalisation (FlexShard section: a few
+ * Newton-Schulz iterations on the whole matrix, each matrix independent).
+ *   X       device, bf16, [batch][m][n] row-major; read, and overwritten with
+ *           the result in the same layout.  m > n is accepted: the iteration
+ *           runs on X^T and the result is written back in X's layout.
+ *   batch   >= 0 (0 is a no-op), m >= 1, n >= 1
+ *   steps   >= 0 (0 = normalisation only)
+ *   coeffs  host pointer to 3 floats (a, b, c); the quintic is
+ *           (3.4445, -4.7750, 2.0315)
+ *   eps     added to the Frobenius norm, eps >= 0 (1e-7 by convention)
+ * Arithmetic: bf16 operands on the tensor cores with fp32 accumulation, fp32
+ * epilogues, and bf16 (round to nearest even) storage of A, B and X between
+ * the steps.  The 1/(||X||_F + eps) factor is applied inside the first
+ * iteration's epilogues, not as a separate pass.
+ * Requirements of the bf16 path: m and n multiples of 8 and X 16-byte
+ * aligned (TMA strides), else MUON_ERR_UNSUPPORTED.
+ * Workspace: muon_ns_batched allocates muon_ns_workspace_bytes() bytes
+ * stream-ordered on `stream` (cudaMallocAsync/cudaFreeAsync from the device's
+ * default memory pool); MUON_ERR_NO_MEMORY if that fails.
+ * muon_ns_batched_ws uses caller memory instead (device, 256-byte aligned,
+ * at least muon_ns_workspace_bytes(); it must not overlap X and must not be
+ * used by other work until the enqueued work has finished).
+ */
+int muon_ns_batched(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3],
+                    float eps, muon_stream_t stream);
+size_t muon_ns_workspace_bytes(int64_t batch, int64_t m, int64_t n);
+int muon_ns_batched_ws(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3],
+                       float eps, void *workspace, size_t workspace_bytes, muon_stream_t stream);
+
+/* fp32 verification mode: the same iteration in plain fp32 FFMA arithmetic
+ * (no TF32, no bf16 rounding), any m, n >= 1; workspace allocated
+ * stream-ordered like muon_ns_batched.  X is device fp32 [batch][m][n]. */
+int muon_ns_batched_f32(float *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3],
+                        float eps, muon_stream_t stream);
+size_t muon_ns_workspace_bytes_f32(int64_t batch, int64_t m, int64_t n);
+
+/* ---------------------------------------------------------------------------
+ * Parameter update with decoupled weight decay (the reading of the update the
+ * page leaves open):
+ *   W <- bf16(fp32(k_w*W) + fp32(k_o*O)),  k_w = fp32(1 - lr*wd),
+ *   k_o = fp32(-lr*scale) (both constants formed in double on the host).
+ *   param   device, bf16, [batch][rows][cols] (read and written in place)
+ *   update  device, bf16, same layout (the orthogonalised O; read)
+ *   scale   <= 0 selects sqrt(max(1, rows/cols)) on the stored shape
+ * Errors: MUON_ERR_INVALID_ARG for null pointers or negative sizes.
+ */
+int muon_apply_update(void *param, const void *update, int64_t batch, int64_t rows, int64_t cols,
+                      float lr, float weight_decay, float scale, muon_stream_t stream);
+
+/* fp32 parameter and update, same formula without the bf16 rounding. */
+int muon_apply_update_f32(float *param, const float *update, int64_t batch, int64_t rows, int64_t cols,
+                          float lr, float weight_decay, float scale, muon_stream_t stream);
+
+/* The default shape scale sqrt(max(1, rows/cols)). */
+float muon_default_scale(int64_t rows, int64_t cols);
+
+/* ---------------------------------------------------------------------------
+ * Status, self-test and tracing helpers.
+ */
+/* Synchronises `stream`, then returns and clears the current device's error
+ * word: MUON_ERR_TIMEOUT if a bounded wait ran out, MUON_ERR_DEVICE for a
+ * failed device-side check, MUON_ERR_CUDA for a CUDA error, else MUON_OK. */
+int muon_get_device_status(muon_stream_t stream);
+
+/* Human-readable name of a muon_status value (static string). */
+const char *muon_status_string(int status);
+
+/* Upper bound, in nanoseconds, on every device-side wait of the tensor-core
+ * kernels (default 2 s).  0 restores the default.  Returns the previous value. */
+uint64_t muon_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/* Launches one kernel that waits on a barrier nothing will complete, with a
+ * wait limit of timeout_ns, so that the timeout path can be checked: the
+ * kernel gives up, records MUON_ERR_TIMEOUT in the error word and returns.
+ * Returns the launch status; read the result with muon_get_device_status(). */
+int muon_selftest_wait_timeout(uint64_t timeout_ns, muon_stream_t stream);
+
+/* Number of kernels this library has launched in this process. */
+int64_t muon_launch_count(void);
+
+/* Tracing: between muon_trace_begin() and muon_trace_end(), every kernel
+ * launch is bracketed by two CUDA events recorded on its own stream.
+ * muon_trace_end() synchronises those events and fills up to max_entries
+ * records (one per kernel kind that launched), returning how many kinds
+ * launched (which may exceed max_entries) or a negative status. */
+typedef struct {
+  const char *kernel;     /* static name of the kernel kind */
+  int64_t launches;       /* launches inside the traced region */
+  double total_ms;        /* summed event-to-event duration */
+} muon_trace_entry;
+
+int muon_trace_begin(void);
+int muon_trace_end(muon_trace_entry *entries, int max_entries);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_H_ */

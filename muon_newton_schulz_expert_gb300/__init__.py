@@ -1,0 +1,276 @@
+"""Python binding of libmuon: the Muon optimizer step on whole matrices, one GB300.
+
+Argument marshalling only: every step runs in the CUDA kernels of
+``_lib/libmuon.so`` (C ABI declared in ``include/muon.h``).  PyTorch supplies
+device memory and the current stream.  There is no fallback: when the library
+has not been built, every call raises ``MuonLibraryMissing``.
+
+Method: "Training a 1T-Parameter MoE on EU public infrastructure with PyTorch
+and TorchTitan", section "FlexShard: Muon without communication" -- one fp32
+state per parameter, a few Newton-Schulz iterations on each whole matrix,
+whole-expert ownership so that the step needs no communication.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libmuon.so")
+
+QUINTIC = (3.4445, -4.7750, 2.0315)
+
+MUON_OK = 0
+STATUS_NAMES = {
+    0: "MUON_OK",
+    -1: "MUON_ERR_INVALID_ARG",
+    -2: "MUON_ERR_UNSUPPORTED",
+    -3: "MUON_ERR_CUDA",
+    -4: "MUON_ERR_NO_MEMORY",
+    -5: "MUON_ERR_TIMEOUT",
+    -6: "MUON_ERR_DEVICE",
+}
+
+# name -> (restype, argtypes) of every symbol declared in include/muon.h
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_INT = ctypes.c_int
+_U64 = ctypes.c_uint64
+_SIZE = ctypes.c_size_t
+
+
+class TraceEntry(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_char_p), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
+
+
+SIGNATURES = {
+    "muon_momentum_update": (_INT, [_P, _P, _P, _I64, _F, _INT, _P]),
+    "muon_momentum_update_f32": (_INT, [_P, _P, _P, _I64, _F, _INT, _P]),
+    "muon_ns_batched": (_INT, [_P, _I64, _I64, _I64, _INT, _P, _F, _P]),
+    "muon_ns_workspace_bytes": (_SIZE, [_I64, _I64, _I64]),
+    "muon_ns_batched_ws": (_INT, [_P, _I64, _I64, _I64, _INT, _P, _F, _P, _SIZE, _P]),
+    "muon_ns_batched_f32": (_INT, [_P, _I64, _I64, _I64, _INT, _P, _F, _P]),
+    "muon_ns_workspace_bytes_f32": (_SIZE, [_I64, _I64, _I64]),
+    "muon_apply_update": (_INT, [_P, _P, _I64, _I64, _I64, _F, _F, _F, _P]),
+    "muon_apply_update_f32": (_INT, [_P, _P, _I64, _I64, _I64, _F, _F, _F, _P]),
+    "muon_default_scale": (_F, [_I64, _I64]),
+    "muon_get_device_status": (_INT, [_P]),
+    "muon_status_string": (ctypes.c_char_p, [_INT]),
+    "muon_set_wait_timeout_ns": (_U64, [_U64]),
+    "muon_selftest_wait_timeout": (_INT, [_U64, _P]),
+    "muon_launch_count": (_I64, []),
+    "muon_trace_begin": (_INT, []),
+    "muon_trace_end": (_INT, [ctypes.POINTER(TraceEntry), _INT]),
+}
+
+
+class MuonLibraryMissing(RuntimeError):
+    pass
+
+
+class MuonError(RuntimeError):
+    def __init__(self, call, status):
+        super().__init__(f"{call} returned {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """The loaded CUDA library (ctypes handle); raises if it was never built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MuonLibraryMissing(
+                f"{LIB_PATH} is missing: build it with muon_newton_schulz_expert_gb300.build.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(name, status):
+    if status != MUON_OK:
+        raise MuonError(name, status)
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _coeffs(coeffs):
+    if len(coeffs) != 3:
+        raise ValueError("coeffs must hold (a, b, c)")
+    return (ctypes.c_float * 3)(*[float(c) for c in coeffs])
+
+
+# ---------------------------------------------------------------------------- the C calls
+def muon_momentum_update(grad, momentum, update_out, mu=0.95, nesterov=True, stream=None):
+    """bf16 grad, fp32 momentum (in place), bf16 update_out; see muon.h."""
+    import torch
+    _need(grad, torch.bfloat16, "grad")
+    _need(momentum, torch.float32, "momentum")
+    _need(update_out, torch.bfloat16, "update_out")
+    if not (grad.numel() == momentum.numel() == update_out.numel()):
+        raise ValueError("grad, momentum and update_out must have the same number of elements")
+    _check("muon_momentum_update", lib().muon_momentum_update(
+        _ptr(grad), _ptr(momentum), _ptr(update_out), grad.numel(), float(mu), int(bool(nesterov)),
+        _stream_handle(stream)))
+
+
+def muon_momentum_update_f32(grad, momentum, update_out, mu=0.95, nesterov=True, stream=None):
+    import torch
+    for t, n in ((grad, "grad"), (momentum, "momentum"), (update_out, "update_out")):
+        _need(t, torch.float32, n)
+    if not (grad.numel() == momentum.numel() == update_out.numel()):
+        raise ValueError("grad, momentum and update_out must have the same number of elements")
+    _check("muon_momentum_update_f32", lib().muon_momentum_update_f32(
+        _ptr(grad), _ptr(momentum), _ptr(update_out), grad.numel(), float(mu), int(bool(nesterov)),
+        _stream_handle(stream)))
+
+
+def _bmn(X):
+    if X.dim() == 2:
+        return 1, X.shape[0], X.shape[1]
+    if X.dim() == 3:
+        return X.shape[0], X.shape[1], X.shape[2]
+    raise ValueError("X must be (m, n) or (batch, m, n)")
+
+
+def muon_ns_workspace_bytes(batch, m, n):
+    return int(lib().muon_ns_workspace_bytes(batch, m, n))
+
+
+def muon_ns_batched(X, steps=5, coeffs=QUINTIC, eps=1e-7, stream=None, workspace=None):
+    """In-place batched Newton-Schulz on a bf16 (batch, m, n) CUDA tensor.
+
+    With ``workspace`` (a CUDA uint8 tensor of at least
+    ``muon_ns_workspace_bytes`` bytes) the ``_ws`` entry point is used.
+    """
+    import torch
+    _need(X, torch.bfloat16, "X")
+    b, m, n = _bmn(X)
+    if workspace is None:
+        st = lib().muon_ns_batched(_ptr(X), b, m, n, int(steps), _coeffs(coeffs), float(eps), _stream_handle(stream))
+        _check("muon_ns_batched", st)
+    else:
+        _need(workspace, torch.uint8, "workspace")
+        st = lib().muon_ns_batched_ws(_ptr(X), b, m, n, int(steps), _coeffs(coeffs), float(eps), _ptr(workspace),
+                                      workspace.numel(), _stream_handle(stream))
+        _check("muon_ns_batched_ws", st)
+    return X
+
+
+def muon_ns_batched_f32(X, steps=5, coeffs=QUINTIC, eps=1e-7, stream=None):
+    """fp32 verification mode of muon_ns_batched (in place)."""
+    import torch
+    _need(X, torch.float32, "X")
+    b, m, n = _bmn(X)
+    _check("muon_ns_batched_f32", lib().muon_ns_batched_f32(
+        _ptr(X), b, m, n, int(steps), _coeffs(coeffs), float(eps), _stream_handle(stream)))
+    return X
+
+
+def muon_apply_update(param, update, lr=0.02, weight_decay=0.1, scale=0.0, stream=None):
+    """param <- (1 - lr*wd) param - lr*scale*update, bf16, in place; scale <= 0: sqrt(max(1, rows/cols))."""
+    import torch
+    _need(param, torch.bfloat16, "param")
+    _need(update, torch.bfloat16, "update")
+    if param.shape != update.shape:
+        raise ValueError("param and update must have the same shape")
+    b, r, c = _bmn(param)
+    _check("muon_apply_update", lib().muon_apply_update(
+        _ptr(param), _ptr(update), b, r, c, float(lr), float(weight_decay), float(scale), _stream_handle(stream)))
+
+
+def muon_apply_update_f32(param, update, lr=0.02, weight_decay=0.1, scale=0.0, stream=None):
+    import torch
+    _need(param, torch.float32, "param")
+    _need(update, torch.float32, "update")
+    if param.shape != update.shape:
+        raise ValueError("param and update must have the same shape")
+    b, r, c = _bmn(param)
+    _check("muon_apply_update_f32", lib().muon_apply_update_f32(
+        _ptr(param), _ptr(update), b, r, c, float(lr), float(weight_decay), float(scale), _stream_handle(stream)))
+
+
+def muon_default_scale(rows, cols):
+    return float(lib().muon_default_scale(rows, cols))
+
+
+def muon_get_device_status(stream=None):
+    return int(lib().muon_get_device_status(_stream_handle(stream)))
+
+
+def muon_status_string(status):
+    return lib().muon_status_string(int(status)).decode()
+
+
+def muon_set_wait_timeout_ns(timeout_ns):
+    return int(lib().muon_set_wait_timeout_ns(int(timeout_ns)))
+
+
+def muon_selftest_wait_timeout(timeout_ns, stream=None):
+    _check("muon_selftest_wait_timeout", lib().muon_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream)))
+
+
+def muon_launch_count():
+    return int(lib().muon_launch_count())
+
+
+def muon_trace_begin():
+    _check("muon_trace_begin", lib().muon_trace_begin())
+
+
+def muon_trace_end():
+    """{kernel name: (launches, total_ms)} for the traced region."""
+    entries = (TraceEntry * 32)()
+    k = lib().muon_trace_end(entries, 32)
+    if k < 0:
+        raise MuonError("muon_trace_end", k)
+    return {entries[i].kernel.decode(): (int(entries[i].launches), float(entries[i].total_ms)) for i in range(min(k, 32))}
+
+
+# ---------------------------------------------------------------------------- one whole step
+def muon_step(params, grads, momenta, update_bufs, *, mu=0.95, nesterov=True, steps=5, coeffs=QUINTIC, eps=1e-7,
+              lr=0.02, weight_decay=0.1, scale=0.0, stream=None):
+    """One Muon step over groups of same-shape matrices.
+
+    Each argument is a list of tensors, one per shape group: params and grads
+    bf16 (batch, rows, cols), momenta fp32 of the same shape, update_bufs bf16
+    scratch of the same shape (receives u, then the orthogonalised update).
+    Per group: momentum -> batched Newton-Schulz -> update.
+    """
+    for p, g, m, u in zip(params, grads, momenta, update_bufs):
+        muon_momentum_update(g, m, u, mu, nesterov, stream)
+        muon_ns_batched(u, steps, coeffs, eps, stream)
+        muon_apply_update(p, u, lr, weight_decay, scale, stream)
+
+
+def default_scale(rows, cols):
+    """sqrt(max(1, rows/cols)) -- host-side convenience, same value as muon_default_scale."""
+    return math.sqrt(max(1.0, rows / cols))

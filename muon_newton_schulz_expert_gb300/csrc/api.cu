@@ -1,0 +1,465 @@
+// C ABI of libmuon: argument checks, workspace layout, the order of the
+// kernels of one Muon step, device status and tracing.
+//
+// Source of the step: "Training a 1T-Parameter MoE on EU public
+// infrastructure with PyTorch and TorchTitan", section "FlexShard: Muon without
+// communication" (one fp32 state per parameter; a few Newton-Schulz iterations
+// on each whole matrix; whole-expert ownership, so no communication).
+#include <math.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+namespace muon {
+
+__device__ unsigned g_muon_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+
+std::mutex g_mu;
+unsigned *g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int64_t> g_launches{0};
+
+const char *kTraceNames[kTraceKinds] = {"momentum_bf16", "momentum_f32", "norm_partial", "norm_final",
+                                        "transpose",     "scale",        "ns_syrk_tc",   "ns_poly_tc",
+                                        "ns_axpy_tc",    "apply_bf16",   "apply_f32",    "gemm_f32",
+                                        "copy",          "selftest_wait"};
+
+struct TraceRec {
+  int kind;
+  cudaEvent_t start, stop;
+};
+
+struct Tracer {
+  bool on = false;
+  std::vector<TraceRec> recs;
+  std::vector<cudaEvent_t> pool;
+  cudaEvent_t pending_start = nullptr;
+} g_trace;
+
+cudaEvent_t take_event() {
+  if (!g_trace.pool.empty()) {
+    cudaEvent_t e = g_trace.pool.back();
+    g_trace.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+// ------------------------------------------------------------ internal services
+void trace_before(int kind, cudaStream_t s) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_trace.on) return;
+  cudaEvent_t e = take_event();
+  if (e && cudaEventRecord(e, s) == cudaSuccess) g_trace.pending_start = e;
+  (void)kind;
+}
+
+int trace_after(int kind, cudaStream_t s) {
+  cudaError_t err = cudaGetLastError();
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_trace.on && g_trace.pending_start) {
+      cudaEvent_t e = take_event();
+      if (e && cudaEventRecord(e, s) == cudaSuccess) g_trace.recs.push_back({kind, g_trace.pending_start, e});
+      g_trace.pending_start = nullptr;
+    }
+  }
+  return err == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+}
+
+unsigned *device_error_word() {
+  int d = current_device();
+  if (d < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[d]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_muon_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[d] = static_cast<unsigned *>(p);
+  }
+  return g_err_ptr[d];
+}
+
+unsigned long long wait_timeout_ns() { return g_timeout_ns.load(); }
+
+int num_sms() {
+  int d = current_device();
+  if (d < 0) return 148;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[d]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || v <= 0) v = 148;
+    g_sms[d] = v;
+  }
+  return g_sms[d];
+}
+
+namespace {
+
+// Workspace of one Newton-Schulz call on [batch][mm][nn] (mm <= nn), in order:
+// two X buffers, A, B (mm x mm each), norm partials, 1/(||X||+eps), its square.
+struct Workspace {
+  void *x1, *x2, *a, *b;
+  float *partial, *inv, *inv2;
+};
+
+size_t ws_bytes(int64_t batch, int64_t mm, int64_t nn, size_t elem) {
+  size_t xs = align256((size_t)batch * mm * nn * elem);
+  size_t as = align256((size_t)batch * mm * mm * elem);
+  size_t fl = align256((size_t)batch * norm_partials() * sizeof(float)) + 2 * align256((size_t)batch * sizeof(float));
+  return 2 * xs + 2 * as + fl;
+}
+
+Workspace carve(void *base, int64_t batch, int64_t mm, int64_t nn, size_t elem) {
+  uint8_t *p = static_cast<uint8_t *>(base);
+  Workspace w{};
+  size_t xs = align256((size_t)batch * mm * nn * elem);
+  size_t as = align256((size_t)batch * mm * mm * elem);
+  w.x1 = p;
+  p += xs;
+  w.x2 = p;
+  p += xs;
+  w.a = p;
+  p += as;
+  w.b = p;
+  p += as;
+  w.partial = reinterpret_cast<float *>(p);
+  p += align256((size_t)batch * norm_partials() * sizeof(float));
+  w.inv = reinterpret_cast<float *>(p);
+  p += align256((size_t)batch * sizeof(float));
+  w.inv2 = reinterpret_cast<float *>(p);
+  return w;
+}
+
+int check_ns_args(const void *X, int64_t batch, int64_t m, int64_t n, int steps, const float *coeffs, float eps) {
+  if (batch < 0 || m < 1 || n < 1 || steps < 0 || !coeffs) return MUON_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || !isfinite(eps)) return MUON_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i)
+    if (!isfinite(coeffs[i])) return MUON_ERR_INVALID_ARG;
+  if (batch > 0 && !X) return MUON_ERR_INVALID_ARG;
+  if (m > (1 << 20) || n > (1 << 20) || batch > (int64_t(1) << 31)) return MUON_ERR_UNSUPPORTED;
+  return MUON_OK;
+}
+
+#define MUON_TRY(expr)          \
+  do {                          \
+    int _st = (expr);           \
+    if (_st != MUON_OK) return _st; \
+  } while (0)
+
+int copy_async(void *dst, const void *src, size_t bytes, cudaStream_t s) {
+  trace_before(kTraceCopy, s);
+  cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+  int st = trace_after(kTraceCopy, s);
+  return e == cudaSuccess ? st : MUON_ERR_CUDA;
+}
+
+// The bf16 iteration on the canonical orientation.  `src0` holds X (mm x nn per
+// matrix).  With `final_dst` set the result ends there (which may be src0
+// itself); with final_dst == nullptr it stays in whichever buffer the last
+// iteration wrote, returned through `result`.
+int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *final_dst, const Workspace &w, int64_t batch, int64_t mm,
+                 int64_t nn, int steps, const float *cf, float eps, cudaStream_t s, __nv_bfloat16 **result) {
+  const int64_t per = mm * nn;
+  MUON_TRY(launch_inv_norm_bf16(src0, batch, per, eps, w.partial, w.inv, w.inv2, s));
+  auto *x1 = static_cast<__nv_bfloat16 *>(w.x1);
+  auto *x2 = static_cast<__nv_bfloat16 *>(w.x2);
+  if (steps == 0) {
+    *result = final_dst ? final_dst : src0;
+    return launch_scale_bf16(src0, *result, batch, per, w.inv, s);
+  }
+  auto *A = static_cast<__nv_bfloat16 *>(w.a);
+  auto *B = static_cast<__nv_bfloat16 *>(w.b);
+  __nv_bfloat16 *src = src0;
+  for (int it = 0; it < steps; ++it) {
+    const bool last = it == steps - 1;
+    __nv_bfloat16 *dst = (src == x1) ? x2 : x1;
+    if (last && final_dst && final_dst != src) dst = final_dst;
+    MUON_TRY(ns_syrk(src, A, batch, mm, nn, it == 0 ? w.inv2 : nullptr, s));
+    MUON_TRY(ns_poly(A, B, batch, mm, cf[1], cf[2], s));
+    MUON_TRY(ns_axpy(B, src, dst, batch, mm, nn, cf[0], it == 0 ? w.inv : nullptr, s));
+    src = dst;
+  }
+  if (final_dst && src != final_dst) {
+    MUON_TRY(copy_async(final_dst, src, (size_t)batch * per * 2, s));
+    src = final_dst;
+  }
+  *result = src;
+  return MUON_OK;
+}
+
+int ns_f32_core(float *src0, float *final_dst, const Workspace &w, int64_t batch, int64_t mm, int64_t nn, int steps,
+                const float *cf, float eps, cudaStream_t s, float **result) {
+  const int64_t per = mm * nn;
+  MUON_TRY(launch_inv_norm_f32(src0, batch, per, eps, w.partial, w.inv, w.inv2, s));
+  auto *x1 = static_cast<float *>(w.x1);
+  auto *x2 = static_cast<float *>(w.x2);
+  if (steps == 0) {
+    *result = final_dst ? final_dst : src0;
+    return launch_scale_f32(src0, *result, batch, per, w.inv, s);
+  }
+  auto *A = static_cast<float *>(w.a);
+  auto *B = static_cast<float *>(w.b);
+  float *src = src0;
+  for (int it = 0; it < steps; ++it) {
+    const bool last = it == steps - 1;
+    float *dst = (src == x1) ? x2 : x1;
+    if (last && final_dst && final_dst != src) dst = final_dst;
+    MUON_TRY(gemm_f32(0, src, nullptr, A, batch, mm, nn, 0.f, 0.f, 0.f, it == 0 ? w.inv2 : nullptr, s));
+    MUON_TRY(gemm_f32(1, A, nullptr, B, batch, mm, mm, 0.f, cf[1], cf[2], nullptr, s));
+    MUON_TRY(gemm_f32(2, B, src, dst, batch, mm, nn, cf[0], 0.f, 0.f, it == 0 ? w.inv : nullptr, s));
+    src = dst;
+  }
+  if (final_dst && src != final_dst) {
+    MUON_TRY(copy_async(final_dst, src, (size_t)batch * per * 4, s));
+    src = final_dst;
+  }
+  *result = src;
+  return MUON_OK;
+}
+
+}  // namespace
+}  // namespace muon
+
+using namespace muon;
+
+extern "C" {
+
+int muon_momentum_update(const void *grad, float *momentum, void *update_out, int64_t numel, float mu, int nesterov,
+                         muon_stream_t stream) {
+  if (numel < 0) return MUON_ERR_INVALID_ARG;
+  if (numel == 0) return MUON_OK;
+  if (!grad || !momentum || !update_out) return MUON_ERR_INVALID_ARG;
+  return launch_momentum_bf16(static_cast<const __nv_bfloat16 *>(grad), momentum,
+                              static_cast<__nv_bfloat16 *>(update_out), numel, mu, nesterov ? 1 : 0,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int muon_momentum_update_f32(const float *grad, float *momentum, float *update_out, int64_t numel, float mu,
+                             int nesterov, muon_stream_t stream) {
+  if (numel < 0) return MUON_ERR_INVALID_ARG;
+  if (numel == 0) return MUON_OK;
+  if (!grad || !momentum || !update_out) return MUON_ERR_INVALID_ARG;
+  return launch_momentum_f32(grad, momentum, update_out, numel, mu, nesterov ? 1 : 0,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t muon_ns_workspace_bytes(int64_t batch, int64_t m, int64_t n) {
+  if (batch <= 0 || m < 1 || n < 1) return 0;
+  return ws_bytes(batch, std::min(m, n), std::max(m, n), 2);
+}
+
+size_t muon_ns_workspace_bytes_f32(int64_t batch, int64_t m, int64_t n) {
+  if (batch <= 0 || m < 1 || n < 1) return 0;
+  return ws_bytes(batch, std::min(m, n), std::max(m, n), 4);
+}
+
+int muon_ns_batched_ws(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3], float eps,
+                       void *workspace, size_t workspace_bytes, muon_stream_t stream) {
+  MUON_TRY(check_ns_args(X, batch, m, n, steps, coeffs, eps));
+  if (batch == 0) return MUON_OK;
+  if (m % 8 || n % 8 || !aligned16(X)) return MUON_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MUON_ERR_INVALID_ARG;
+  if (workspace_bytes < muon_ns_workspace_bytes(batch, m, n)) return MUON_ERR_NO_MEMORY;
+  if (!device_error_word()) return MUON_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const float cf[3] = {coeffs[0], coeffs[1], coeffs[2]};
+  const int64_t mm = std::min(m, n), nn = std::max(m, n);
+  Workspace w = carve(workspace, batch, mm, nn, 2);
+  auto *x = static_cast<__nv_bfloat16 *>(X);
+  __nv_bfloat16 *res = nullptr;
+  if (m <= n) return ns_bf16_core(x, x, w, batch, mm, nn, steps, cf, eps, s, &res);
+  // m > n: iterate on X^T (n x m) in the workspace and transpose the result
+  // back into X from whichever buffer the last iteration wrote.
+  auto *xt = static_cast<__nv_bfloat16 *>(w.x1);
+  MUON_TRY(launch_transpose_bf16(x, xt, batch, m, n, s));
+  MUON_TRY(ns_bf16_core(xt, nullptr, w, batch, mm, nn, steps, cf, eps, s, &res));
+  return launch_transpose_bf16(res, x, batch, mm, nn, s);
+}
+
+int muon_ns_batched(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3], float eps,
+                    muon_stream_t stream) {
+  MUON_TRY(check_ns_args(X, batch, m, n, steps, coeffs, eps));
+  if (batch == 0) return MUON_OK;
+  if (m % 8 || n % 8 || !aligned16(X)) return MUON_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t bytes = muon_ns_workspace_bytes(batch, m, n);
+  void *ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess || !ws) {
+    cudaGetLastError();
+    return MUON_ERR_NO_MEMORY;
+  }
+  int st = muon_ns_batched_ws(X, batch, m, n, steps, coeffs, eps, ws, bytes, stream);
+  cudaError_t fe = cudaFreeAsync(ws, s);
+  if (st == MUON_OK && fe != cudaSuccess) st = MUON_ERR_CUDA;
+  return st;
+}
+
+int muon_ns_batched_f32(float *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3], float eps,
+                        muon_stream_t stream) {
+  MUON_TRY(check_ns_args(X, batch, m, n, steps, coeffs, eps));
+  if (batch == 0) return MUON_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t bytes = muon_ns_workspace_bytes_f32(batch, m, n);
+  void *ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess || !ws) {
+    cudaGetLastError();
+    return MUON_ERR_NO_MEMORY;
+  }
+  const float cf[3] = {coeffs[0], coeffs[1], coeffs[2]};
+  const int64_t mm = std::min(m, n), nn = std::max(m, n);
+  Workspace w = carve(ws, batch, mm, nn, 4);
+  int st;
+  float *res = nullptr;
+  if (m <= n) {
+    st = ns_f32_core(X, X, w, batch, mm, nn, steps, cf, eps, s, &res);
+  } else {
+    float *xt = static_cast<float *>(w.x1);
+    st = launch_transpose_f32(X, xt, batch, m, n, s);
+    if (st == MUON_OK) st = ns_f32_core(xt, nullptr, w, batch, mm, nn, steps, cf, eps, s, &res);
+    if (st == MUON_OK) st = launch_transpose_f32(res, X, batch, mm, nn, s);
+  }
+  cudaError_t fe = cudaFreeAsync(ws, s);
+  if (st == MUON_OK && fe != cudaSuccess) st = MUON_ERR_CUDA;
+  return st;
+}
+
+float muon_default_scale(int64_t rows, int64_t cols) {
+  if (rows < 1 || cols < 1) return 1.0f;
+  return (float)sqrt(std::max(1.0, (double)rows / (double)cols));
+}
+
+static void update_constants(int64_t rows, int64_t cols, float lr, float wd, float scale, float *kw, float *ko) {
+  const double sc = scale > 0.f ? (double)scale : sqrt(std::max(1.0, (double)rows / (double)cols));
+  *kw = (float)(1.0 - (double)lr * (double)wd);
+  *ko = (float)(-(double)lr * sc);
+}
+
+int muon_apply_update(void *param, const void *update, int64_t batch, int64_t rows, int64_t cols, float lr,
+                      float weight_decay, float scale, muon_stream_t stream) {
+  if (batch < 0 || rows < 0 || cols < 0) return MUON_ERR_INVALID_ARG;
+  const int64_t numel = batch * rows * cols;
+  if (numel == 0) return MUON_OK;
+  if (!param || !update || !isfinite(lr) || !isfinite(weight_decay) || !isfinite(scale)) return MUON_ERR_INVALID_ARG;
+  float kw, ko;
+  update_constants(rows, cols, lr, weight_decay, scale, &kw, &ko);
+  return launch_apply_bf16(static_cast<__nv_bfloat16 *>(param), static_cast<const __nv_bfloat16 *>(update), numel,
+                           kw, ko, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int muon_apply_update_f32(float *param, const float *update, int64_t batch, int64_t rows, int64_t cols, float lr,
+                          float weight_decay, float scale, muon_stream_t stream) {
+  if (batch < 0 || rows < 0 || cols < 0) return MUON_ERR_INVALID_ARG;
+  const int64_t numel = batch * rows * cols;
+  if (numel == 0) return MUON_OK;
+  if (!param || !update || !isfinite(lr) || !isfinite(weight_decay) || !isfinite(scale)) return MUON_ERR_INVALID_ARG;
+  float kw, ko;
+  update_constants(rows, cols, lr, weight_decay, scale, &kw, &ko);
+  return launch_apply_f32(param, update, numel, kw, ko, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int muon_get_device_status(muon_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MUON_ERR_CUDA;
+  unsigned *p = device_error_word();
+  if (!p) return MUON_ERR_CUDA;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MUON_ERR_CUDA;
+  if (v && cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return MUON_ERR_CUDA;
+  if (v & kErrTimeout) return MUON_ERR_TIMEOUT;
+  if (v & kErrDevice) return MUON_ERR_DEVICE;
+  return MUON_OK;
+}
+
+const char *muon_status_string(int status) {
+  switch (status) {
+    case MUON_OK: return "MUON_OK";
+    case MUON_ERR_INVALID_ARG: return "MUON_ERR_INVALID_ARG";
+    case MUON_ERR_UNSUPPORTED: return "MUON_ERR_UNSUPPORTED";
+    case MUON_ERR_CUDA: return "MUON_ERR_CUDA";
+    case MUON_ERR_NO_MEMORY: return "MUON_ERR_NO_MEMORY";
+    case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT";
+    case MUON_ERR_DEVICE: return "MUON_ERR_DEVICE";
+    default: return "MUON_ERR_UNKNOWN";
+  }
+}
+
+uint64_t muon_set_wait_timeout_ns(uint64_t timeout_ns) {
+  return g_timeout_ns.exchange(timeout_ns ? timeout_ns : kDefaultTimeoutNs);
+}
+
+int muon_selftest_wait_timeout(uint64_t timeout_ns, muon_stream_t stream) {
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull) return MUON_ERR_INVALID_ARG;
+  if (!device_error_word()) return MUON_ERR_CUDA;
+  return selftest_wait(timeout_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int64_t muon_launch_count(void) { return g_launches.load(); }
+
+int muon_trace_begin(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_trace.on = true;
+  return MUON_OK;
+}
+
+int muon_trace_end(muon_trace_entry *entries, int max_entries) {
+  std::vector<TraceRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_trace.on = false;
+    recs.swap(g_trace.recs);
+    if (g_trace.pending_start) {
+      g_trace.pool.push_back(g_trace.pending_start);
+      g_trace.pending_start = nullptr;
+    }
+  }
+  int64_t launches[kTraceKinds] = {};
+  double ms[kTraceKinds] = {};
+  int st = MUON_OK;
+  for (const TraceRec &r : recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+      st = MUON_ERR_CUDA;
+    launches[r.kind] += 1;
+    ms[r.kind] += t;
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (const TraceRec &r : recs) {
+      g_trace.pool.push_back(r.start);
+      g_trace.pool.push_back(r.stop);
+    }
+  }
+  if (st != MUON_OK) return st;
+  int kinds = 0;
+  for (int k = 0; k < kTraceKinds; ++k) {
+    if (!launches[k]) continue;
+    if (entries && kinds < max_entries) entries[kinds] = {kTraceNames[k], launches[k], ms[k]};
+    ++kinds;
+  }
+  return kinds;
+}
+
+}  // extern "C"

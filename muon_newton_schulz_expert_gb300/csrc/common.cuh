@@ -1,0 +1,89 @@
+// Internal declarations shared by the libmuon translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "muon.h"
+
+namespace muon {
+
+// Bits of the device error word.
+constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrDevice = 2u;
+
+// Kernel kinds known to the tracer (index into kTraceNames).
+enum TraceKind : int {
+  kTraceMomentum = 0,
+  kTraceMomentumF32,
+  kTraceNormPartial,
+  kTraceNormFinal,
+  kTraceTranspose,
+  kTraceScale,
+  kTraceSyrk,      // A = s^2 X X^T   (tensor cores)
+  kTracePoly,      // B = b A + c A A (tensor cores)
+  kTraceAxpy,      // X' = s (a X + B X) (tensor cores)
+  kTraceApply,
+  kTraceApplyF32,
+  kTraceGemmF32,
+  kTraceCopy,
+  kTraceSelftest,
+  kTraceKinds
+};
+
+// Called around every kernel launch (cheap when tracing is off).
+void trace_before(int kind, cudaStream_t s);
+int trace_after(int kind, cudaStream_t s);   // checks cudaGetLastError; returns a muon_status
+
+// Device address of the error word of the current device (never null after success).
+unsigned *device_error_word();
+unsigned long long wait_timeout_ns();
+int num_sms();
+
+// ---- elementwise / reduction kernels (elementwise.cu) ----
+int launch_momentum_bf16(const __nv_bfloat16 *g, float *buf, __nv_bfloat16 *u, int64_t numel, float mu,
+                         int nesterov, cudaStream_t s);
+int launch_momentum_f32(const float *g, float *buf, float *u, int64_t numel, float mu, int nesterov,
+                        cudaStream_t s);
+int launch_apply_bf16(__nv_bfloat16 *w, const __nv_bfloat16 *o, int64_t numel, float kw, float ko,
+                      cudaStream_t s);
+int launch_apply_f32(float *w, const float *o, int64_t numel, float kw, float ko, cudaStream_t s);
+// Per-matrix inverse norm: inv[b] = 1/(||X_b||_F + eps), inv2[b] = inv[b]^2.
+// `partial` holds batch*norm_partials() floats of scratch.
+int norm_partials();
+int launch_inv_norm_bf16(const __nv_bfloat16 *x, int64_t batch, int64_t per, float eps, float *partial,
+                         float *inv, float *inv2, cudaStream_t s);
+int launch_inv_norm_f32(const float *x, int64_t batch, int64_t per, float eps, float *partial, float *inv,
+                        float *inv2, cudaStream_t s);
+// dst[b] = src[b]^T for [batch][rows][cols] -> [batch][cols][rows]
+int launch_transpose_bf16(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int64_t batch, int64_t rows,
+                          int64_t cols, cudaStream_t s);
+int launch_transpose_f32(const float *src, float *dst, int64_t batch, int64_t rows, int64_t cols,
+                         cudaStream_t s);
+// dst[b] = scale[b] * src[b] (per matrix of `per` elements); src may equal dst
+int launch_scale_bf16(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int64_t batch, int64_t per,
+                      const float *scale, cudaStream_t s);
+int launch_scale_f32(const float *src, float *dst, int64_t batch, int64_t per, const float *scale,
+                     cudaStream_t s);
+
+// ---- tensor-core GEMMs of one Newton-Schulz iteration (gemm_tc.cu) ----
+// All matrices are batched, densely packed, bf16 row-major; X is m x n (m <= n).
+// A = s2[b] * X X^T          (s2 == nullptr: 1), upper triangle computed, mirrored
+int ns_syrk(const __nv_bfloat16 *X, __nv_bfloat16 *A, int64_t batch, int64_t m, int64_t n, const float *s2,
+            cudaStream_t s);
+// B = b*A + c*A A            (A symmetric), upper triangle computed, mirrored
+int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, float b, float c,
+            cudaStream_t s);
+// Xn = s1[b] * (a*X + B X)   (s1 == nullptr: 1)
+int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, __nv_bfloat16 *Xn, int64_t batch, int64_t m,
+            int64_t n, float a, const float *s1, cudaStream_t s);
+int selftest_wait(unsigned long long timeout_ns, cudaStream_t s);
+
+// ---- fp32 SIMT GEMMs for the verification mode (gemm_f32.cu) ----
+// mode 0: C = s2 * P P^T (P m x k);  mode 1: C = b*P + c*P P (P m x m);
+// mode 2: C = s1 * (a*Q + P Q) (P m x m, Q m x n)
+int gemm_f32(int mode, const float *P, const float *Q, float *C, int64_t batch, int64_t m, int64_t n,
+             float a, float b, float c, const float *scale, cudaStream_t s);
+
+}  // namespace muon

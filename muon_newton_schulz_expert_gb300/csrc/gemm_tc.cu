@@ -1,0 +1,604 @@
+// Tensor-core GEMMs of one Newton-Schulz iteration on sm_103a.
+//
+// Source: "Training a 1T-Parameter MoE on EU public infrastructure with
+// PyTorch and TorchTitan", section "FlexShard: Muon without communication":
+// Newton-Schulz iterations on whole expert matrices, each matrix owned by one
+// rank.  With X m x n (m <= n) one iteration is
+//   A  = X X^T            (symmetric m x m: upper triangle computed, mirrored)
+//   B  = b A + c A A      (A symmetric, so A A = A A^T: same kernel shape)
+//   X' = a X + B X        (full m x n)
+// The first iteration also applies the Frobenius factor s = 1/(||X||_F+eps):
+// A gets s^2, X' gets s (so X0 = s X is never stored).
+//
+// Design (one persistent CTA per SM, 192 threads, warp-specialised):
+//   warp 0 lane 0  TMA producer: 128x64 and 256x64 bf16 tiles with 128-byte
+//                  swizzle into a 4-stage shared-memory ring (mbarrier
+//                  complete_tx);
+//   warp 1         TMEM allocation (512 columns = two 128x256 fp32
+//                  accumulators); lane 0 issues tcgen05.mma (M=128, N=256,
+//                  K=16, bf16 in, fp32 accumulate) and tcgen05.commit;
+//   warps 2..5     epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//                  lanes 32*(w%4)..+31), fp32 epilogue math, bf16 stores.
+// The double-buffered accumulator lets the epilogue of tile t overlap the
+// main loop of tile t+1.  Every mbarrier wait is bounded: when it runs out the
+// kernel records a timeout in the device error word, raises a shared abort
+// flag so the other roles stop, lets in-flight copies land, frees its TMEM and
+// returns.  No cluster multicast is used: each CTA loads its own tiles.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace muon {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int NUM_BARS = 2 * STAGES + 5;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + NUM_BARS * 8 + 16;
+constexpr int THREADS = 192;
+constexpr int ACC_COLS = BN;
+constexpr int TMEM_COLS = 2 * ACC_COLS;
+
+enum Epi { EPI_SYRK = 0, EPI_POLY = 1, EPI_AXPY = 2 };
+
+struct Params {
+  int M, N, K;                 // output M x N, reduction length K (per matrix)
+  int tiles_m, tiles_n;
+  int tiles_per_mat;
+  long long num_tiles;
+  __nv_bfloat16 *out;
+  long long out_ld, out_mat;   // row stride and matrix stride in elements
+  const __nv_bfloat16 *src;    // epilogue operand (A for POLY, X for AXPY)
+  long long src_ld, src_mat;
+  const float *scale;          // per-matrix factor (SYRK: s^2, AXPY: s) or null
+  float a, b, c;
+  unsigned *err;
+  unsigned long long timeout_ns;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+struct Watch {
+  volatile int *abort;
+  unsigned *err;
+  unsigned long long limit_ns;
+};
+
+// Bounded wait for the phase of `bar` with the given parity to complete.
+// Returns false (and stops waiting) on timeout or when another role aborted.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Watch w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*w.abort) return false;
+      if (global_ns() - t0 > w.limit_ns) {
+        *w.abort = 1;
+        atomicOr(w.err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns -> 32 registers per thread, waited.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: start address, leading and stride byte
+// offsets, descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, A K-major,
+// B K-major or MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+// Tile t -> (matrix, row tile, column tile).  Symmetric outputs enumerate, per
+// matrix, the tiles that hold at least one element on or above the diagonal:
+// row tile i covers rows [128i, 128i+128) and needs column tiles j >= i/2.
+template <int EPI>
+__device__ __forceinline__ void decode_tile(const Params &p, long long t, int &mat, int &ti, int &tj) {
+  mat = (int)(t / p.tiles_per_mat);
+  int r = (int)(t - (long long)mat * p.tiles_per_mat);
+  if (EPI == EPI_AXPY) {
+    tj = r / p.tiles_m;
+    ti = r - tj * p.tiles_m;
+  } else {
+    int i = 0;
+    for (;;) {
+      int cnt = p.tiles_n - (i >> 1);
+      if (r < cnt) break;
+      r -= cnt;
+      ++i;
+    }
+    ti = i;
+    tj = (i >> 1) + r;
+  }
+}
+
+union Pack8 {
+  uint4 v;
+  __nv_bfloat162 h[4];
+};
+
+template <int EPI, bool B_MN>
+__global__ void __launch_bounds__(THREADS, 1)
+    ns_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#define FULL(s) (bar0 + 8u * (uint32_t)(s))
+#define EMPTY(s) (bar0 + 8u * (uint32_t)(STAGES + (s)))
+#define ACCF(a) (bar0 + 8u * (uint32_t)(2 * STAGES + (a)))
+#define ACCE(a) (bar0 + 8u * (uint32_t)(2 * STAGES + 2 + (a)))
+  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(FULL(s), 1);
+      mbar_init(EMPTY(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(ACCF(a), 1);
+      mbar_init(ACCE(a), 4 * 32);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Watch w{abort_flag, p.err, p.timeout_ns};
+  const int num_kb = (p.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (long long t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        int mat, ti, tj;
+        decode_tile<EPI>(p, t, mat, ti, tj);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(EMPTY(stage), phase ^ 1u, w)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(FULL(stage), STAGE_BYTES);
+          const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_STAGE;
+          tma_load_3d(sa, &tmA, FULL(stage), kb * BK, ti * BM, mat);
+          if (!B_MN) {
+            tma_load_3d(sb, &tmB, FULL(stage), kb * BK, tj * BN, mat);
+          } else {
+#pragma unroll
+            for (int q = 0; q < BN / 64; ++q) tma_load_3d(sb + q * (64 * BK * 2), &tmB, FULL(stage), tj * BN + q * 64, kb * BK, mat);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(BM, BN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (long long t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        if (!wait_bounded(ACCE(acc), acc_phase ^ 1u, w)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(acc * ACC_COLS);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(FULL(stage), phase, w)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t adesc = smem_desc(sa + kk * (UMMA_K * 2), 16, 1024);
+            const uint64_t bdesc = B_MN ? smem_desc(sb + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
+                                        : smem_desc(sb + kk * (UMMA_K * 2), 16, 1024);
+            tc_mma(d, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(EMPTY(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(ACCF(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // all MMAs issued by this thread have completed once drain_bar flips
+      tc_commit(drain_bar);
+      Watch wd{abort_flag, p.err, p.timeout_ns};
+      volatile int no_abort = 0;
+      wd.abort = &no_abort;
+      wait_bounded(drain_bar, 0, wd);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quadrant accessible to this warp
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (long long t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      int mat, ti, tj;
+      decode_tile<EPI>(p, t, mat, ti, tj);
+      const bool ok = wait_bounded(ACCF(acc), acc_phase, w);
+      if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: the TMEM loads below are .sync.aligned
+      tc_fence_after();
+      const int row = ti * BM + q * 32 + lane;
+      const bool row_ok = row < p.M;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
+      const float sc = p.scale ? p.scale[mat] : 1.0f;
+      __nv_bfloat16 *outm = p.out + (long long)mat * p.out_mat;
+      const __nv_bfloat16 *srcm = p.src ? p.src + (long long)mat * p.src_mat : nullptr;
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(taddr + (uint32_t)(ch * 32), r);
+        const int col0 = tj * BN + ch * 32;
+        if (!row_ok || col0 >= p.N) continue;
+        float v[32];
+        if (EPI == EPI_SYRK) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = sc * __uint_as_float(r[k]);
+        } else {
+          // a*X + acc (AXPY) or b*A + c*acc (POLY), reading the epilogue operand row
+          const __nv_bfloat16 *srow = srcm + (long long)row * p.src_ld + col0;
+          const bool full_chunk = col0 + 32 <= p.N;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            Pack8 s8;
+            if (full_chunk) {
+              s8.v = __ldg(reinterpret_cast<const uint4 *>(srow) + g);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                int c0 = col0 + g * 8 + 2 * e;
+                float lo = c0 < p.N ? __bfloat162float(srow[g * 8 + 2 * e]) : 0.f;
+                float hi = c0 + 1 < p.N ? __bfloat162float(srow[g * 8 + 2 * e + 1]) : 0.f;
+                s8.h[e] = __floats2bfloat162_rn(lo, hi);
+              }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float2 f = __bfloat1622float2(s8.h[e]);
+              const int k = g * 8 + 2 * e;
+              if (EPI == EPI_AXPY) {
+                v[k] = sc * fmaf(p.a, f.x, __uint_as_float(r[k]));
+                v[k + 1] = sc * fmaf(p.a, f.y, __uint_as_float(r[k + 1]));
+              } else {
+                v[k] = fmaf(p.c, __uint_as_float(r[k]), p.b * f.x);
+                v[k + 1] = fmaf(p.c, __uint_as_float(r[k + 1]), p.b * f.y);
+              }
+            }
+          }
+        }
+        __nv_bfloat16 *orow = outm + (long long)row * p.out_ld;
+        if (EPI == EPI_AXPY) {
+          if (col0 + 32 <= p.N) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              Pack8 o;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) o.h[e] = __floats2bfloat162_rn(v[g * 8 + 2 * e], v[g * 8 + 2 * e + 1]);
+              reinterpret_cast<uint4 *>(orow + col0)[g] = o.v;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (col0 + k < p.N) orow[col0 + k] = __float2bfloat16_rn(v[k]);
+          }
+        } else {
+          // symmetric output: (row, c) for c >= row, and the mirror (c, row) for c > row
+          if (col0 >= row && col0 + 32 <= p.N) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              Pack8 o;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) o.h[e] = __floats2bfloat162_rn(v[g * 8 + 2 * e], v[g * 8 + 2 * e + 1]);
+              reinterpret_cast<uint4 *>(orow + col0)[g] = o.v;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int c = col0 + k;
+              if (c >= row && c < p.N) orow[c] = __float2bfloat16_rn(v[k]);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int c = col0 + k;
+            if (c > row && c < p.N) outm[(long long)c * p.out_ld + row] = __float2bfloat16_rn(v[k]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(ACCE(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+#undef FULL
+#undef EMPTY
+#undef ACCF
+#undef ACCE
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // let copies already in flight land before the shared memory is released
+    const unsigned long long t0 = global_ns();
+    while (global_ns() - t0 < 200000ull) __nanosleep(1000);
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+__global__ void selftest_wait_kernel(unsigned *err, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // phase 0 of `bar` never completes: nothing arrives on it
+  wait_bounded(smem_u32(&bar), 0, Watch{&abort_flag, err, limit_ns});
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 3-D map over a dense [batch][rows][cols] bf16 stack; box = 64 columns x box_rows rows x 1 matrix.
+int make_map(CUtensorMap *map, const void *base, int64_t batch, int64_t rows, int64_t cols, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return MUON_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(rows * cols * 2)};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MUON_OK : MUON_ERR_CUDA;
+}
+
+template <int EPI, bool B_MN>
+int launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int trace_kind, cudaStream_t s) {
+  if (p.num_tiles == 0) return MUON_OK;
+  static std::once_flag attr_once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
+  cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once[dev & 63], [&] {
+    attr_err = cudaFuncSetAttribute(ns_gemm_kernel<EPI, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return MUON_ERR_CUDA;
+  const long long grid = std::min<long long>(p.num_tiles, num_sms());
+  trace_before(trace_kind, s);
+  ns_gemm_kernel<EPI, B_MN><<<(unsigned)grid, THREADS, SMEM_BYTES, s>>>(ma, mb, p);
+  return trace_after(trace_kind, s);
+}
+
+Params base_params(int M, int N, int K, int64_t batch) {
+  Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.tiles_m = (M + BM - 1) / BM;
+  p.tiles_n = (N + BN - 1) / BN;
+  p.err = device_error_word();
+  p.timeout_ns = wait_timeout_ns();
+  (void)batch;
+  return p;
+}
+
+int triangle_tiles(int tiles_m, int tiles_n) {
+  int total = 0;
+  for (int i = 0; i < tiles_m; ++i) total += tiles_n - (i >> 1);
+  return total;
+}
+
+}  // namespace
+
+int ns_syrk(const __nv_bfloat16 *X, __nv_bfloat16 *A, int64_t batch, int64_t m, int64_t n, const float *s2,
+            cudaStream_t s) {
+  CUtensorMap ma, mb;
+  int st = make_map(&ma, X, batch, m, n, BM);
+  if (!st) st = make_map(&mb, X, batch, m, n, BN);
+  if (st) return st;
+  Params p = base_params((int)m, (int)m, (int)n, batch);
+  p.tiles_per_mat = triangle_tiles(p.tiles_m, p.tiles_n);
+  p.num_tiles = (long long)p.tiles_per_mat * batch;
+  p.out = A;
+  p.out_ld = m;
+  p.out_mat = m * m;
+  p.scale = s2;
+  return launch<EPI_SYRK, false>(ma, mb, p, kTraceSyrk, s);
+}
+
+int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, float b, float c, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  int st = make_map(&ma, A, batch, m, m, BM);
+  if (!st) st = make_map(&mb, A, batch, m, m, BN);
+  if (st) return st;
+  Params p = base_params((int)m, (int)m, (int)m, batch);
+  p.tiles_per_mat = triangle_tiles(p.tiles_m, p.tiles_n);
+  p.num_tiles = (long long)p.tiles_per_mat * batch;
+  p.out = B;
+  p.out_ld = m;
+  p.out_mat = m * m;
+  p.src = A;
+  p.src_ld = m;
+  p.src_mat = m * m;
+  p.b = b;
+  p.c = c;
+  return launch<EPI_POLY, false>(ma, mb, p, kTracePoly, s);
+}
+
+int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, __nv_bfloat16 *Xn, int64_t batch, int64_t m, int64_t n,
+            float a, const float *s1, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  int st = make_map(&ma, B, batch, m, m, BM);
+  if (!st) st = make_map(&mb, X, batch, m, n, 64);
+  if (st) return st;
+  Params p = base_params((int)m, (int)n, (int)m, batch);
+  p.tiles_per_mat = p.tiles_m * p.tiles_n;
+  p.num_tiles = (long long)p.tiles_per_mat * batch;
+  p.out = Xn;
+  p.out_ld = n;
+  p.out_mat = m * n;
+  p.src = X;
+  p.src_ld = n;
+  p.src_mat = m * n;
+  p.a = a;
+  p.scale = s1;
+  return launch<EPI_AXPY, true>(ma, mb, p, kTraceAxpy, s);
+}
+
+int selftest_wait(unsigned long long timeout_ns, cudaStream_t s) {
+  trace_before(kTraceSelftest, s);
+  selftest_wait_kernel<<<1, 32, 0, s>>>(device_error_word(), timeout_ns);
+  return trace_after(kTraceSelftest, s);
+}
+
+}  // namespace muon

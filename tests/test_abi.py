@@ -1,0 +1,110 @@
+"""The C ABI library builds, loads and exports every declared symbol (CPU only:
+no call below reaches the GPU; argument errors are returned before any CUDA
+call is made)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import muon_newton_schulz_expert_gb300 as mk
+from muon_newton_schulz_expert_gb300 import build as mkbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "muon.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(muon_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mkbuild.build()
+    return mk.lib()
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("muon_momentum_update", "muon_ns_batched", "muon_apply_update"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    names = declared_functions()
+    assert set(names) == set(mk.SIGNATURES), set(names) ^ set(mk.SIGNATURES)
+    raw = ctypes.CDLL(mkbuild.LIB)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_library_is_built_for_sm103a_only():
+    assert mkbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings(lib):
+    for code, name in mk.STATUS_NAMES.items():
+        assert mk.muon_status_string(code) == name
+    assert mk.muon_status_string(-99) == "MUON_ERR_UNKNOWN"
+
+
+def test_default_scale_host_function(lib):
+    assert abs(mk.muon_default_scale(6144, 1792) - 1.8516402) < 1e-6
+    assert mk.muon_default_scale(1792, 6144) == 1.0
+    assert mk.muon_default_scale(0, 5) == 1.0
+
+
+def test_argument_errors_are_returned_without_touching_the_gpu(lib):
+    c3 = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+    # negative sizes, null pointers, bad eps, null coefficients
+    assert lib.muon_ns_batched(None, 1, 8, 8, 5, c3, 1e-7, None) == -1
+    assert lib.muon_ns_batched(None, -1, 8, 8, 5, c3, 1e-7, None) == -1
+    assert lib.muon_ns_batched(ctypes.c_void_p(256), 1, 0, 8, 5, c3, 1e-7, None) == -1
+    assert lib.muon_ns_batched(ctypes.c_void_p(256), 1, 8, 8, -1, c3, 1e-7, None) == -1
+    assert lib.muon_ns_batched(ctypes.c_void_p(256), 1, 8, 8, 5, None, 1e-7, None) == -1
+    assert lib.muon_ns_batched(ctypes.c_void_p(256), 1, 8, 8, 5, c3, -1.0, None) == -1
+    assert lib.muon_ns_batched(ctypes.c_void_p(256), 1, 8, 8, 5, c3, float("nan"), None) == -1
+    bad = (ctypes.c_float * 3)(float("inf"), 0, 0)
+    assert lib.muon_ns_batched(ctypes.c_void_p(256), 1, 8, 8, 5, bad, 1e-7, None) == -1
+    # shapes and alignment the tensor-core path does not take
+    assert lib.muon_ns_batched(ctypes.c_void_p(256), 1, 12, 16, 5, c3, 1e-7, None) == -2
+    assert lib.muon_ns_batched(ctypes.c_void_p(258), 1, 16, 16, 5, c3, 1e-7, None) == -2
+    assert lib.muon_ns_batched(ctypes.c_void_p(256), 1, 1 << 21, 8, 5, c3, 1e-7, None) == -2
+    # batch 0 is a no-op even with a null pointer
+    assert lib.muon_ns_batched(None, 0, 8, 8, 5, c3, 1e-7, None) == 0
+    assert lib.muon_ns_batched_f32(None, 0, 3, 5, 5, c3, 1e-7, None) == 0
+    # workspace checks of the _ws variant (alignment, size)
+    need = lib.muon_ns_workspace_bytes(2, 64, 128)
+    assert need > 2 * 2 * 64 * 128 * 2
+    assert lib.muon_ns_batched_ws(ctypes.c_void_p(256), 2, 64, 128, 5, c3, 1e-7, ctypes.c_void_p(4096 + 16), need,
+                                  None) == -1
+    assert lib.muon_ns_batched_ws(ctypes.c_void_p(256), 2, 64, 128, 5, c3, 1e-7, ctypes.c_void_p(4096), need - 1,
+                                  None) == -4
+    # elementwise calls
+    assert lib.muon_momentum_update(None, None, None, -1, 0.9, 1, None) == -1
+    assert lib.muon_momentum_update(None, None, None, 10, 0.9, 1, None) == -1
+    assert lib.muon_momentum_update(None, None, None, 0, 0.9, 1, None) == 0
+    assert lib.muon_apply_update(None, None, 1, 4, -4, 0.02, 0.1, 0.0, None) == -1
+    assert lib.muon_apply_update(None, None, 1, 4, 4, 0.02, 0.1, 0.0, None) == -1
+    assert lib.muon_apply_update(None, None, 0, 4, 4, 0.02, 0.1, 0.0, None) == 0
+    assert lib.muon_selftest_wait_timeout(0, None) == -1
+
+
+def test_workspace_size_formula(lib):
+    # two X buffers, A and B, plus small per-matrix scalars; orientation-free
+    b, m, n = 96, 1792, 6144
+    got = lib.muon_ns_workspace_bytes(b, m, n)
+    core = 2 * b * m * n * 2 + 2 * b * m * m * 2
+    assert core <= got <= core + 64 * 1024
+    assert lib.muon_ns_workspace_bytes(b, n, m) == got
+    assert lib.muon_ns_workspace_bytes(0, m, n) == 0
+    assert lib.muon_ns_workspace_bytes_f32(b, m, n) >= 2 * core
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(mk, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(mk, "_lib", None)
+    with pytest.raises(mk.MuonLibraryMissing):
+        mk.lib()
