@@ -1,0 +1,386 @@
+"""Benchmark of the Muon step on one rank's batch of MoE expert matrices.
+
+Workload (per GPU): 32 experts of the model-configuration table of "Training a
+1T-Parameter MoE on EU public infrastructure with PyTorch and TorchTitan"
+(hidden 6144, expert hidden 1792): 64 matrices stored 6144 x 1792 (w1, w3) and
+32 stored 1792 x 6144 (w2), bf16 gradients N(0,1) times a per-row log-normal
+factor, fp32 momentum, bf16 parameters.  One step = momentum over all 96
+matrices, one batched Newton-Schulz call per stored shape (5 quintic steps),
+and the parameter update: the whole path.  Each rank owns whole matrices
+(section "FlexShard: Muon without communication"), so ranks share nothing and
+the scaling is weak: N GPUs process N x 96 matrices per step.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle instead, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Muon NS step: 1792×6144 expert matrices/s; TFLOP/s vs GB300 bf16 tensor peak"
+UNIT = "matrices/s"
+WORKLOAD = "rank_expert_batch_96: 64 x 6144x1792 (w1,w3) + 32 x 1792x6144 (w2) bf16, fp32 momentum, 5 quintic NS steps"
+QUINTIC = (3.4445, -4.7750, 2.0315)
+MU, LR, WD, EPS = 0.95, 0.02, 0.1, 1e-7
+M_EXP, N_EXP = 1792, 6144
+# algorithmic work per 1792 x 6144 matrix and NS iteration (symmetry-aware):
+# A = X X^T takes m^2 n, B = bA + cAA takes m^3, X' = aX + BX takes 2 m^2 n
+FLOPS_SYRK = M_EXP * M_EXP * N_EXP
+FLOPS_POLY = M_EXP ** 3
+FLOPS_AXPY = 2 * M_EXP * M_EXP * N_EXP
+FLOPS_NS = 5 * (FLOPS_SYRK + FLOPS_POLY + FLOPS_AXPY)        # 3.247e11
+FLOPS_NS_DENSE = 5 * (4 * M_EXP * M_EXP * N_EXP + 2 * M_EXP ** 3)
+KERNEL_FLOPS = {"ns_syrk_tc": FLOPS_SYRK, "ns_poly_tc": FLOPS_POLY, "ns_axpy_tc": FLOPS_AXPY}
+PER_MATRIX_ELEMS = M_EXP * N_EXP
+# algorithmic HBM bytes per element of the elementwise kernels
+KERNEL_BYTES = {"momentum_bf16": 12, "apply_bf16": 6, "norm_partial": 2, "transpose": 4}
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def init_dist(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("gloo")
+    return dist
+
+
+def max_over_ranks(dist, value):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_gpu(args):
+    import torch
+
+    import muon_newton_schulz_expert_gb300 as mk
+    from muon_newton_schulz_expert_gb300 import build as mkbuild
+    import workloads
+
+    rank, world, local = dist_env()
+    dist = init_dist(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mkbuild.build()
+    mk.lib()
+
+    groups = [(64, workloads.HIDDEN, workloads.EXPERT_HIDDEN), (32, workloads.EXPERT_HIDDEN, workloads.HIDDEN)]
+    total = sum(c for c, _, _ in groups)
+    numel = total * PER_MATRIX_ELEMS
+    seed0 = 1234 + 3000 + 7919 * rank
+
+    def split(flat):
+        views, off = [], 0
+        for c, r, k in groups:
+            views.append(flat[off:off + c * r * k].view(c, r, k))
+            off += c * r * k
+        return views
+
+    params = torch.empty(numel, dtype=torch.bfloat16, device=dev)
+    for i, (v, (c, r, k)) in enumerate(zip(split(params), groups)):
+        v.copy_(workloads.parameters(c, r, k, seed0 + 10 * i + 1, device=dev))
+    grads = []
+    for s in range(2):   # two gradient sets alternate between steps
+        g = torch.empty(numel, dtype=torch.bfloat16, device=dev)
+        for i, (v, (c, r, k)) in enumerate(zip(split(g), groups)):
+            v.copy_(workloads.gradients(c, r, k, seed0 + 100000 * s + 10 * i, device=dev))
+        grads.append(g)
+    momentum = torch.zeros(numel, dtype=torch.float32, device=dev)
+    upd = torch.empty(numel, dtype=torch.bfloat16, device=dev)
+    p_views, u_views = split(params), split(upd)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(k):
+        mk.muon_momentum_update(grads[k % 2], momentum, upd, MU, True, stream)
+        for u in u_views:
+            mk.muon_ns_batched(u, 5, QUINTIC, EPS, stream)
+        for p, u in zip(p_views, u_views):
+            mk.muon_apply_update(p, u, LR, WD, 0.0, stream)
+
+    for k in range(args.warmup):
+        step(k)
+    if mk.muon_get_device_status() != 0:
+        raise RuntimeError("device status not OK after warm-up")
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = mk.muon_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    mk.muon_trace_begin()
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    trace = mk.muon_trace_end()
+    launches = mk.muon_launch_count() - launches0
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    barrier(dist)
+    ms_max = max_over_ranks(dist, ms)
+    if mk.muon_get_device_status() != 0:
+        raise RuntimeError("device status not OK after the timed steps")
+
+    # end to end: host gradients in, host parameters out, every step
+    e2e = None
+    if not args.no_e2e:
+        host_g = torch.empty(numel, dtype=torch.bfloat16, pin_memory=True)
+        host_g.copy_(grads[0].cpu())
+        host_p = torch.empty(numel, dtype=torch.bfloat16, pin_memory=True)
+        for k in range(2):
+            grads[0].copy_(host_g, non_blocking=True)
+            step(0)
+            host_p.copy_(params, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        barrier(dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ke = max(3, args.steps // 2)
+        e0.record(stream)
+        for k in range(ke):
+            grads[0].copy_(host_g, non_blocking=True)
+            step(0)
+            host_p.copy_(params, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / ke)
+        e2e = {"value": round(total * world / (e_ms / 1e3), 3), "unit": UNIT, "ms_per_step": round(e_ms, 3),
+               "h2d_bytes_per_step": numel * 2, "d2h_bytes_per_step": numel * 2, "steps": ke}
+
+    peaks, peak_src = load_peaks()
+    kernels = {}
+    for name, (n, t) in sorted(trace.items()):
+        ent = {"launches": n, "avg_ms": round(t / n, 4), "share": None}
+        if name in KERNEL_FLOPS:   # every matrix passes through each tensor kernel 5 times per step
+            flops = KERNEL_FLOPS[name] * 5 * total * args.steps
+            ent["tflops"] = round(flops / (t / 1e3) / 1e12, 1)
+        if name in KERNEL_BYTES:
+            passes = 2 if name == "transpose" else 1
+            nbytes = KERNEL_BYTES[name] * PER_MATRIX_ELEMS * args.steps * (total if name != "transpose" else 64 * passes)
+            ent["gbs"] = round(nbytes / (t / 1e3) / 1e9, 1)
+        kernels[name] = ent
+    traced_ms = sum(t for _, t in trace.values())
+    for name, (n, t) in trace.items():
+        kernels[name]["share"] = round(t / traced_ms, 4) if traced_ms else None
+    ns_ms = sum(trace.get(k, (0, 0.0))[1] for k in ("ns_syrk_tc", "ns_poly_tc", "ns_axpy_tc", "norm_partial",
+                                                        "norm_final", "transpose")) / args.steps
+    dom = max(KERNEL_FLOPS, key=lambda k: trace.get(k, (0, 0.0))[1])
+    dn, dt = trace[dom]
+    achieved = KERNEL_FLOPS[dom] * 5 * total * args.steps / (dt / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": args.traffic,
+            "peak_source": f"bf16_tflops_sustained ({peak_src})",
+            "avg_launch_ms": round(dt / dn, 4), "launches": dn}
+    tc_ms = sum(trace.get(k, (0, 0.0))[1] for k in KERNEL_FLOPS) / args.steps
+    value = total * world / (ms_max / 1e3)
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the pages' expert matrices)",
+        "config": {"workload": WORKLOAD, "matrices_per_gpu": total, "ns_steps": 5, "coeffs": list(QUINTIC),
+                   "mu": MU, "lr": LR, "weight_decay": WD, "eps": EPS,
+                   "l2": "inputs larger than L2 (2.1 GB bf16 gradients + 4.2 GB fp32 momentum per step)",
+                   "parallelism": f"whole-matrix ownership, {world} independent replica(s), no collective"},
+        "ns_tflops": round(total * FLOPS_NS / (ns_ms / 1e3) / 1e12, 1) if ns_ms else None,
+        "step_tflops": round(total * FLOPS_NS / (ms / 1e3) / 1e12, 1),
+        "tensor_kernels_tflops": round(total * FLOPS_NS / (tc_ms / 1e3) / 1e12, 1) if tc_ms else None,
+        "flops_per_matrix": {"algorithmic_symmetric": FLOPS_NS, "dense_equivalent": FLOPS_NS_DENSE},
+        "roofline": roof, "kernels": kernels, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- the oracle on the host cores
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def oracle_sample(rank_seed=0):
+    """One w1-shaped (6144 x 1792) and one w2-shaped (1792 x 6144) matrix with full step inputs."""
+    import torch
+    import workloads
+    out = []
+    for i, (r, c) in enumerate(((workloads.HIDDEN, workloads.EXPERT_HIDDEN), (workloads.EXPERT_HIDDEN, workloads.HIDDEN))):
+        g = workloads.gradients(1, r, c, 9000 + rank_seed + i).float().numpy()
+        w = workloads.parameters(1, r, c, 9100 + rank_seed + i).float().numpy()
+        out.append((g, w))
+    return out
+
+
+def oracle_step_matrix(g, w):
+    import numpy as np
+    from oracle import muon_oracle as O
+    buf = np.zeros_like(g, dtype=np.float32)
+    return O.muon_step(w, g, buf, mu=MU, lr=LR, weight_decay=WD, eps=EPS)
+
+
+def cpu_baseline(seconds):
+    sample = oracle_sample()
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        for g, w in sample:
+            oracle_step_matrix(g, w)
+            done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done / dt, 4), "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{done} matrices (alternating 6144x1792 and 1792x6144), full step (momentum, 5 NS steps, "
+                      f"update) in fp64 numpy, {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    sample = oracle_sample()
+    for k in range(args.warmup):
+        oracle_step_matrix(*sample[k % 2])
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        oracle_step_matrix(*sample[k % 2])
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    cores = oracle_threads()
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; shapes of the pages' expert matrices)",
+        "config": {"workload": WORKLOAD, "reference": "fp64 CPU oracle; each step is one matrix of the workload"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} single-matrix steps alternating 6144x1792 / 1792x6144"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per launch of the dominant kernel from an ncu capture, if current")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
