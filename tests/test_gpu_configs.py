@@ -1,0 +1,150 @@
+"""Full-size workloads on the GPU, in the launch configuration bench.py times.
+
+Every matrix of a shape group goes through one batched call; the oracle then
+recomputes sampled matrices one by one (fp64, same bf16 inputs).  Momentum is
+compared bit for bit, the Newton-Schulz output within 2e-2 relative Frobenius
+error, the updated parameters against the update formula applied to the GPU's
+own orthogonalised update (bit-exact) and against the fp64 chain (within one
+bf16 ulp plus lr*scale times the update difference).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import muon_oracle as O
+from tests._util import bits16, bits32, np32, rel_fro, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 2e-2
+LR, WD, MU = float(np.float32(0.02)), float(np.float32(0.1)), float(np.float32(0.95))
+
+
+@pytest.fixture(scope="module")
+def mk():
+    return require_gpu()
+
+
+def step_groups(mk, cfg_index, groups, W, buf, u, step):
+    grads = []
+    for gi, grp in enumerate(groups):
+        g = workloads.gradients(grp.count, grp.rows, grp.cols, workloads.seed_for(cfg_index, step, gi, 0),
+                                device="cuda", kind=workloads.CONFIGS[cfg_index].grad_kind)
+        grads.append(g)
+    snap = [(np32(w), np32(b)) for w, b in zip(W, buf)]
+    for gi in range(len(groups)):
+        mk.muon_momentum_update(grads[gi], buf[gi], u[gi], mu=MU)
+    u_in = [u_.clone() for u_ in u]
+    for gi in range(len(groups)):
+        mk.muon_ns_batched(u[gi])
+    for gi in range(len(groups)):
+        mk.muon_apply_update(W[gi], u[gi], lr=LR, weight_decay=WD)
+    assert mk.muon_get_device_status() == 0
+    return grads, snap, u_in
+
+
+def check_matrix(g, W_prev, b_prev, buf_new, u_in, O_gpu, W_new, rows, cols):
+    nb, uu = O.momentum_update(np32(g), b_prev, MU, True)
+    assert np.array_equal(bits32(buf_new), nb.view(np.uint32))
+    assert np.array_equal(bits16(u_in), O.bf16_bits(uu))
+    want = O.newton_schulz(O.bf16_round(uu))
+    Og = np32(O_gpu)
+    err = rel_fro(Og, want)
+    assert err < BF16_TOL, err
+    sc = O.default_scale(rows, cols)
+    exact = O.apply_update_fp32(W_prev, Og, LR, WD, sc)
+    assert np.array_equal(bits16(W_new), O.bf16_bits(exact))
+    chain = O.apply_update(W_prev, want, LR, WD, sc)
+    ulp = np.abs(W_prev) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(np32(W_new) - chain) <= ulp + LR * sc * np.abs(Og - want) + 1e-7)
+    return err
+
+
+def test_config2_one_expert_three_steps(mk):
+    cfg = workloads.CONFIGS[2]
+    groups = cfg.groups
+    W = [workloads.parameters(g.count, g.rows, g.cols, workloads.seed_for(2, 0, gi, 1), device="cuda")
+         for gi, g in enumerate(groups)]
+    buf = [torch.zeros(g.count, g.rows, g.cols, device="cuda") for g in groups]
+    u = [torch.empty(g.count, g.rows, g.cols, dtype=torch.bfloat16, device="cuda") for g in groups]
+    errs = []
+    for step in range(cfg.steps):
+        grads, snap, u_in = step_groups(mk, 2, groups, W, buf, u, step)
+        for gi, grp in enumerate(groups):
+            for i in range(grp.count):
+                errs.append(check_matrix(grads[gi][i], snap[gi][0][i], snap[gi][1][i], buf[gi][i], u_in[gi][i],
+                                         u[gi][i], W[gi][i], grp.rows, grp.cols))
+    print("config2 rel errors", ["%.3e" % e for e in errs])
+
+
+def test_config3_rank_batch_sampled(mk):
+    cfg = workloads.CONFIGS[3]
+    groups = cfg.groups
+    W = [workloads.parameters(g.count, g.rows, g.cols, workloads.seed_for(3, 0, gi, 1), device="cuda")
+         for gi, g in enumerate(groups)]
+    buf = [torch.zeros(g.count, g.rows, g.cols, device="cuda") for g in groups]
+    u = [torch.empty(g.count, g.rows, g.cols, dtype=torch.bfloat16, device="cuda") for g in groups]
+    grads, snap, u_in = step_groups(mk, 3, groups, W, buf, u, 0)
+    samples = {0: (0, 37, 63), 1: (0, 31)}
+    for gi, idx in samples.items():
+        grp = groups[gi]
+        for i in idx:
+            err = check_matrix(grads[gi][i], snap[gi][0][i], snap[gi][1][i], buf[gi][i], u_in[gi][i], u[gi][i],
+                               W[gi][i], grp.rows, grp.cols)
+            print(f"config3 group {gi} matrix {i}: rel {err:.3e}")
+    # every matrix of the batch: finite and of the quintic's scale (||O||_F^2 / m within the map's range)
+    for gi, grp in enumerate(groups):
+        m = min(grp.rows, grp.cols)
+        fro2 = (u[gi].float() ** 2).sum(dim=(1, 2)) / m
+        assert torch.isfinite(fro2).all() and (fro2 > 0.3).all() and (fro2 < 1.3).all()
+
+
+def test_config4_dense_projections_sampled(mk):
+    cfg = workloads.CONFIGS[4]
+    groups = cfg.groups
+    X = [workloads.gradients(g.count, g.rows, g.cols, workloads.seed_for(4, 0, gi, 0), device="cuda", kind="normal")
+         for gi, g in enumerate(groups)]
+    X_in = [x.clone() for x in X]
+    for x in X:
+        mk.muon_ns_batched(x)
+    assert mk.muon_get_device_status() == 0
+    for gi, i in ((0, 5), (1, 2)):
+        want = O.newton_schulz(np32(X_in[gi][i]))
+        err = rel_fro(np32(X[gi][i]), want)
+        print(f"config4 group {gi} matrix {i}: rel {err:.3e}")
+        assert err < BF16_TOL
+
+
+def test_config5_conditioning_stress_sampled(mk):
+    cfg = workloads.CONFIGS[5]
+    grp = cfg.groups[0]
+    m, n = grp.rows, grp.cols
+    G = workloads.spectrum_batch(grp.count, m, n, device="cuda", dtype=torch.float32)
+    G_in = G.clone()
+    mk.muon_ns_batched(G)
+    assert mk.muon_get_device_status() == 0
+    assert torch.isfinite(G.float()).all()
+    eps = 1e-7
+    for i in (0, 7, 100):
+        want = O.newton_schulz(np32(G_in[i]))
+        got = np32(G[i])
+        err = rel_fro(got, want)
+        print(f"config5 matrix {i}: rel {err:.3e}")
+        assert err < BF16_TOL
+        # the output singular values follow the scalar quintic map on the known spectrum
+        U, s, V = workloads.spectrum_factors(m, n, i, device="cuda", dtype=torch.float32)
+        U, s, V = U.double().cpu().numpy(), s.double().cpu().numpy(), V.double().cpu().numpy()
+        s0 = s / (math.sqrt(float(np.sum(s * s))) + eps)
+        p = s0.copy()
+        for _ in range(5):
+            p = 3.4445 * p - 4.7750 * p ** 3 + 2.0315 * p ** 5
+        core = np.diag(U.T @ got.astype(np.float64) @ V)
+        big = s0 >= 1e-2
+        assert big.sum() > 10
+        assert np.max(np.abs(core[big] - p[big])) < 5e-2
+        if i % 10 == 0:
+            assert np.all(s[64:] == 0)
