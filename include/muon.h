@@ -104,6 +104,33 @@ size_t muon_ns_workspace_bytes(int64_t batch, int64_t m, int64_t n);
 int muon_ns_batched_ws(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3],
                        float eps, void *workspace, size_t workspace_bytes, muon_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Newton-Schulz that allocates nothing.  The paper has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory -- a host
+ * that owns all device memory through its own arena and forbids allocations by
+ * the libraries it loads, a runtime with a fixed memory budget that must not
+ * allocate after start-up, or a plain C caller without a device allocator.
+ * It computes exactly what muon_ns_batched computes (same kernels, same
+ * arguments, same errors) on a scratch array of MUON_NS_STATIC_SCRATCH_BYTES
+ * that the library reserves statically on the device.
+ *   - Limit: muon_ns_workspace_bytes(batch, m, n) must not exceed
+ *     MUON_NS_STATIC_SCRATCH_BYTES (64 MiB: one 1792 x 6144 expert matrix per
+ *     call); larger calls return MUON_ERR_NO_MEMORY and touch nothing.
+ *   - The scratch stays resident on every GPU that loads the library until
+ *     the process exits.
+ *   - The first call on a device looks up the scratch's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one scratch array, which keeps the last call's
+ *     contents (no part of it needs to start at zero).  Calls whose work
+ *     overlaps on the GPU -- on different streams or from different host
+ *     threads -- race on it: issue them on one stream.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+#define MUON_NS_STATIC_SCRATCH_BYTES (64ull << 20)
+int muon_ns_batched_static(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3],
+                           float eps, muon_stream_t stream);
+
 /* fp32 verification mode: the same iteration in plain fp32 FFMA arithmetic
  * (no TF32, no bf16 rounding), any m, n >= 1; workspace allocated
  * stream-ordered like muon_ns_batched.  X is device fp32 [batch][m][n]. */

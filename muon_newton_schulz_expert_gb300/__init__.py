@@ -52,6 +52,7 @@ SIGNATURES = {
     "muon_ns_batched": (_INT, [_P, _I64, _I64, _I64, _INT, _P, _F, _P]),
     "muon_ns_workspace_bytes": (_SIZE, [_I64, _I64, _I64]),
     "muon_ns_batched_ws": (_INT, [_P, _I64, _I64, _I64, _INT, _P, _F, _P, _SIZE, _P]),
+    "muon_ns_batched_static": (_INT, [_P, _I64, _I64, _I64, _INT, _P, _F, _P]),
     "muon_ns_batched_f32": (_INT, [_P, _I64, _I64, _I64, _INT, _P, _F, _P]),
     "muon_ns_workspace_bytes_f32": (_SIZE, [_I64, _I64, _I64]),
     "muon_apply_update": (_INT, [_P, _P, _I64, _I64, _I64, _F, _F, _F, _P]),
@@ -182,6 +183,24 @@ def muon_ns_batched(X, steps=5, coeffs=QUINTIC, eps=1e-7, stream=None, workspace
         st = lib().muon_ns_batched_ws(_ptr(X), b, m, n, int(steps), _coeffs(coeffs), float(eps), _ptr(workspace),
                                       workspace.numel(), _stream_handle(stream))
         _check("muon_ns_batched_ws", st)
+    return X
+
+
+NS_STATIC_SCRATCH_BYTES = 64 << 20
+
+
+def muon_ns_batched_static(X, steps=5, coeffs=QUINTIC, eps=1e-7, stream=None):
+    """muon_ns_batched on the library's static device scratch: allocates nothing.
+
+    For callers that cannot allocate device memory.  At most
+    NS_STATIC_SCRATCH_BYTES of workspace per call (one 1792 x 6144 expert
+    matrix); calls that overlap on the GPU share the scratch and race.
+    """
+    import torch
+    _need(X, torch.bfloat16, "X")
+    b, m, n = _bmn(X)
+    _check("muon_ns_batched_static", lib().muon_ns_batched_static(
+        _ptr(X), b, m, n, int(steps), _coeffs(coeffs), float(eps), _stream_handle(stream)))
     return X
 
 
