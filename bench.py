@@ -166,7 +166,10 @@ def run_gpu(args):
     mkbuild.build()
     mk.lib()
 
-    groups = [(64, workloads.HIDDEN, workloads.EXPERT_HIDDEN), (32, workloads.EXPERT_HIDDEN, workloads.HIDDEN)]
+    if args.workload == "profile8":   # small case for ncu captures: 8 w2-shaped matrices (176 MB, > L2)
+        groups = [(8, workloads.EXPERT_HIDDEN, workloads.HIDDEN)]
+    else:
+        groups = [(64, workloads.HIDDEN, workloads.EXPERT_HIDDEN), (32, workloads.EXPERT_HIDDEN, workloads.HIDDEN)]
     total = sum(c for c, _, _ in groups)
     numel = total * PER_MATRIX_ELEMS
     seed0 = rank_seed_base(rank)
@@ -260,7 +263,8 @@ def run_gpu(args):
             ent["tflops"] = round(flops / (t / 1e3) / 1e12, 1)
         if name in KERNEL_BYTES:
             passes = 2 if name == "transpose" else 1
-            nbytes = KERNEL_BYTES[name] * PER_MATRIX_ELEMS * args.steps * (total if name != "transpose" else 64 * passes)
+            ntr = sum(c for c, r, k in groups if r > k)
+            nbytes = KERNEL_BYTES[name] * PER_MATRIX_ELEMS * args.steps * (total if name != "transpose" else ntr * passes)
             ent["gbs"] = round(nbytes / (t / 1e3) / 1e9, 1)
         kernels[name] = ent
     traced_ms = sum(t for _, t in trace.values())
@@ -282,7 +286,8 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the pages' expert matrices)",
-        "config": {"workload": WORKLOAD, "matrices_per_gpu": total, "ns_steps": 5, "coeffs": list(QUINTIC),
+        "config": {"workload": WORKLOAD if args.workload == "rank96" else
+                   "profile8: 8 x 1792x6144 bf16 (ncu capture case, not a bench line)", "matrices_per_gpu": total, "ns_steps": 5, "coeffs": list(QUINTIC),
                    "mu": MU, "lr": LR, "weight_decay": WD, "eps": EPS,
                    "l2": "inputs larger than L2 (2.1 GB bf16 gradients + 4.2 GB fp32 momentum per step)",
                    "parallelism": f"whole-matrix ownership, {world} independent replica(s), no collective"},
@@ -382,6 +387,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--workload", default="rank96", choices=["rank96", "profile8"],
+                    help="rank96: the 96-matrix bench workload; profile8: 8 matrices for ncu captures")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture, if current")
     args = ap.parse_args()

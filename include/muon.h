@@ -86,8 +86,9 @@ int muon_momentum_update_f32(const float *grad, float *momentum, float *update_o
  *           (3.4445, -4.7750, 2.0315)
  *   eps     added to the Frobenius norm, eps >= 0 (1e-7 by convention)
  * Arithmetic: bf16 operands on the tensor cores with fp32 accumulation, fp32
- * epilogues, and bf16 (round to nearest even) storage of A, B and X between
- * the steps.  The 1/(||X||_F + eps) factor is applied inside the first
+ * epilogues, bf16 (round to nearest even) storage of A and B, and X carried
+ * between the steps as two bf16 halves (hi = bf16(X), lo = bf16(X - hi)):
+ * the tensor cores read hi, the a*X term uses hi + lo.  The 1/(||X||_F + eps) factor is applied inside the first
  * iteration's epilogues, not as a separate pass.
  * Requirements of the bf16 path: m and n multiples of 8 and X 16-byte
  * aligned (TMA strides), else MUON_ERR_UNSUPPORTED.
@@ -114,7 +115,7 @@ int muon_ns_batched_ws(void *X, int64_t batch, int64_t m, int64_t n, int steps, 
  * arguments, same errors) on a scratch array of MUON_NS_STATIC_SCRATCH_BYTES
  * that the library reserves statically on the device.
  *   - Limit: muon_ns_workspace_bytes(batch, m, n) must not exceed
- *     MUON_NS_STATIC_SCRATCH_BYTES (64 MiB: one 1792 x 6144 expert matrix per
+ *     MUON_NS_STATIC_SCRATCH_BYTES (96 MiB: one 1792 x 6144 expert matrix per
  *     call); larger calls return MUON_ERR_NO_MEMORY and touch nothing.
  *   - The scratch stays resident on every GPU that loads the library until
  *     the process exits.
@@ -127,7 +128,7 @@ int muon_ns_batched_ws(void *X, int64_t batch, int64_t m, int64_t n, int steps, 
  *     threads -- race on it: issue them on one stream.
  *   - No cudaMalloc, cudaFree or other allocating routine is called.
  */
-#define MUON_NS_STATIC_SCRATCH_BYTES (64ull << 20)
+#define MUON_NS_STATIC_SCRATCH_BYTES (96ull << 20)
 int muon_ns_batched_static(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3],
                            float eps, muon_stream_t stream);
 

@@ -186,7 +186,7 @@ def muon_ns_batched(X, steps=5, coeffs=QUINTIC, eps=1e-7, stream=None, workspace
     return X
 
 
-NS_STATIC_SCRATCH_BYTES = 64 << 20
+NS_STATIC_SCRATCH_BYTES = 96 << 20
 
 
 def muon_ns_batched_static(X, steps=5, coeffs=QUINTIC, eps=1e-7, stream=None):

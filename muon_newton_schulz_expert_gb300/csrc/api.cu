@@ -120,9 +120,10 @@ int num_sms() {
 namespace {
 
 // Workspace of one Newton-Schulz call on [batch][mm][nn] (mm <= nn), in order:
-// two X buffers, A, B (mm x mm each), norm partials, 1/(||X||+eps), its square.
+// two X buffers, the low half of X (bf16 path only), A, B (mm x mm each), norm
+// partials, 1/(||X||+eps) and its square.
 struct Workspace {
-  void *x1, *x2, *a, *b;
+  void *x1, *x2, *lo, *a, *b;
   float *partial, *inv, *inv2;
 };
 
@@ -130,7 +131,7 @@ size_t ws_bytes(int64_t batch, int64_t mm, int64_t nn, size_t elem) {
   size_t xs = align256((size_t)batch * mm * nn * elem);
   size_t as = align256((size_t)batch * mm * mm * elem);
   size_t fl = align256((size_t)batch * norm_partials() * sizeof(float)) + 2 * align256((size_t)batch * sizeof(float));
-  return 2 * xs + 2 * as + fl;
+  return (elem == 2 ? 3 : 2) * xs + 2 * as + fl;
 }
 
 Workspace carve(void *base, int64_t batch, int64_t mm, int64_t nn, size_t elem) {
@@ -142,6 +143,10 @@ Workspace carve(void *base, int64_t batch, int64_t mm, int64_t nn, size_t elem) 
   p += xs;
   w.x2 = p;
   p += xs;
+  if (elem == 2) {
+    w.lo = p;
+    p += xs;
+  }
   w.a = p;
   p += as;
   w.b = p;
@@ -193,6 +198,7 @@ int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *final_dst, const Workspace 
   }
   auto *A = static_cast<__nv_bfloat16 *>(w.a);
   auto *B = static_cast<__nv_bfloat16 *>(w.b);
+  auto *lo = static_cast<__nv_bfloat16 *>(w.lo);
   __nv_bfloat16 *src = src0;
   for (int it = 0; it < steps; ++it) {
     const bool last = it == steps - 1;
@@ -200,7 +206,9 @@ int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *final_dst, const Workspace 
     if (last && final_dst && final_dst != src) dst = final_dst;
     MUON_TRY(ns_syrk(src, A, batch, mm, nn, it == 0 ? w.inv2 : nullptr, s));
     MUON_TRY(ns_poly(A, B, batch, mm, cf[1], cf[2], s));
-    MUON_TRY(ns_axpy(B, src, dst, batch, mm, nn, cf[0], it == 0 ? w.inv : nullptr, s));
+    // the input X is exactly bf16 (no low half); the result leaves as bf16
+    MUON_TRY(ns_axpy(B, src, it == 0 ? nullptr : lo, dst, last ? nullptr : lo, batch, mm, nn, cf[0],
+                     it == 0 ? w.inv : nullptr, s));
     src = dst;
   }
   if (final_dst && src != final_dst) {

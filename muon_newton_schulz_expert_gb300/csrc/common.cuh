@@ -75,9 +75,11 @@ int ns_syrk(const __nv_bfloat16 *X, __nv_bfloat16 *A, int64_t batch, int64_t m, 
 // B = b*A + c*A A            (A symmetric), upper triangle computed, mirrored
 int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, float b, float c,
             cudaStream_t s);
-// Xn = s1[b] * (a*X + B X)   (s1 == nullptr: 1)
-int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, __nv_bfloat16 *Xn, int64_t batch, int64_t m,
-            int64_t n, float a, const float *s1, cudaStream_t s);
+// Xn = s1[b] * (a*X + B X)   (s1 == nullptr: 1), with X = X + X_lo and the
+// result split into Xn = bf16(result), Xn_lo = bf16(result - Xn); X_lo and
+// Xn_lo may be null (zero low half / not wanted) and may be the same buffer
+int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *Xn,
+            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, cudaStream_t s);
 int selftest_wait(unsigned long long timeout_ns, cudaStream_t s);
 
 // ---- fp32 SIMT GEMMs for the verification mode (gemm_f32.cu) ----

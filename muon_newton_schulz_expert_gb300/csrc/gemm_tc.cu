@@ -9,6 +9,13 @@
 //   X' = a X + B X        (full m x n)
 // The first iteration also applies the Frobenius factor s = 1/(||X||_F+eps):
 // A gets s^2, X' gets s (so X0 = s X is never stored).
+// X is carried between iterations as a pair of bf16 halves, hi = bf16(X) and
+// lo = bf16(X - hi): the tensor cores read hi only, while the a X term of the
+// epilogue uses hi + lo.  Rounding X itself to bf16 would inject noise of
+// relative size 2^-9 into every singular direction each iteration, and the
+// quintic multiplies small singular values by up to a = 3.4445 per step, so
+// on rank-deficient or ill-conditioned inputs that noise grows to ~10% of the
+// output; with the lo half it stays near 2^-17.
 //
 // Design (one persistent CTA per SM, 192 threads, warp-specialised):
 //   warp 0 lane 0  TMA producer: 128x64 and 256x64 bf16 tiles with 128-byte
@@ -59,6 +66,10 @@ struct Params {
   const __nv_bfloat16 *src;    // epilogue operand (A for POLY, X for AXPY)
   long long src_ld, src_mat;
   const float *scale;          // per-matrix factor (SYRK: s^2, AXPY: s) or null
+  // AXPY only: low halves of X (X = hi + lo, hi = bf16(X), lo = bf16(X - hi));
+  // read at the element the thread then writes, so one buffer serves in place
+  const __nv_bfloat16 *src_lo;
+  __nv_bfloat16 *out_lo;
   float a, b, c;
   unsigned *err;
   unsigned long long timeout_ns;
@@ -363,21 +374,28 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = sc * __uint_as_float(r[k]);
         } else {
-          // a*X + acc (AXPY) or b*A + c*acc (POLY), reading the epilogue operand row
-          const __nv_bfloat16 *srow = srcm + (long long)row * p.src_ld + col0;
+          // a*X + acc (AXPY, X = hi + lo) or b*A + c*acc (POLY), reading the epilogue operand row
+          const long long eoff = (long long)row * p.src_ld + col0;
+          const __nv_bfloat16 *srow = srcm + eoff;
+          const __nv_bfloat16 *lrow =
+              (EPI == EPI_AXPY && p.src_lo) ? p.src_lo + (long long)mat * p.src_mat + eoff : nullptr;
           const bool full_chunk = col0 + 32 <= p.N;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            Pack8 s8;
+            Pack8 s8, l8;
             if (full_chunk) {
               s8.v = __ldg(reinterpret_cast<const uint4 *>(srow) + g);
+              // plain load: the lo buffer may be the one this thread overwrites below
+              l8.v = lrow ? reinterpret_cast<const uint4 *>(lrow)[g] : make_uint4(0u, 0u, 0u, 0u);
             } else {
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                int c0 = col0 + g * 8 + 2 * e;
-                float lo = c0 < p.N ? __bfloat162float(srow[g * 8 + 2 * e]) : 0.f;
-                float hi = c0 + 1 < p.N ? __bfloat162float(srow[g * 8 + 2 * e + 1]) : 0.f;
-                s8.h[e] = __floats2bfloat162_rn(lo, hi);
+                const int k0 = g * 8 + 2 * e;
+                const bool ok0 = col0 + k0 < p.N, ok1 = col0 + k0 + 1 < p.N;
+                s8.h[e] = __floats2bfloat162_rn(ok0 ? __bfloat162float(srow[k0]) : 0.f,
+                                                ok1 ? __bfloat162float(srow[k0 + 1]) : 0.f);
+                l8.h[e] = __floats2bfloat162_rn(ok0 && lrow ? __bfloat162float(lrow[k0]) : 0.f,
+                                                ok1 && lrow ? __bfloat162float(lrow[k0 + 1]) : 0.f);
               }
             }
 #pragma unroll
@@ -385,8 +403,9 @@ __global__ void __launch_bounds__(THREADS, 1)
               float2 f = __bfloat1622float2(s8.h[e]);
               const int k = g * 8 + 2 * e;
               if (EPI == EPI_AXPY) {
-                v[k] = sc * fmaf(p.a, f.x, __uint_as_float(r[k]));
-                v[k + 1] = sc * fmaf(p.a, f.y, __uint_as_float(r[k + 1]));
+                const float2 fl = __bfloat1622float2(l8.h[e]);
+                v[k] = sc * fmaf(p.a, f.x + fl.x, __uint_as_float(r[k]));
+                v[k + 1] = sc * fmaf(p.a, f.y + fl.y, __uint_as_float(r[k + 1]));
               } else {
                 v[k] = fmaf(p.c, __uint_as_float(r[k]), p.b * f.x);
                 v[k + 1] = fmaf(p.c, __uint_as_float(r[k + 1]), p.b * f.y);
@@ -396,18 +415,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __nv_bfloat16 *orow = outm + (long long)row * p.out_ld;
         if (EPI == EPI_AXPY) {
+          __nv_bfloat16 *lout = p.out_lo ? p.out_lo + (long long)mat * p.out_mat + (long long)row * p.out_ld : nullptr;
           if (col0 + 32 <= p.N) {
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-              Pack8 o;
+              Pack8 o, ol;
 #pragma unroll
-              for (int e = 0; e < 4; ++e) o.h[e] = __floats2bfloat162_rn(v[g * 8 + 2 * e], v[g * 8 + 2 * e + 1]);
+              for (int e = 0; e < 4; ++e) {
+                const int k = g * 8 + 2 * e;
+                o.h[e] = __floats2bfloat162_rn(v[k], v[k + 1]);
+                const float2 h = __bfloat1622float2(o.h[e]);
+                ol.h[e] = __floats2bfloat162_rn(v[k] - h.x, v[k + 1] - h.y);
+              }
               reinterpret_cast<uint4 *>(orow + col0)[g] = o.v;
+              if (lout) reinterpret_cast<uint4 *>(lout + col0)[g] = ol.v;
             }
           } else {
 #pragma unroll
             for (int k = 0; k < 32; ++k)
-              if (col0 + k < p.N) orow[col0 + k] = __float2bfloat16_rn(v[k]);
+              if (col0 + k < p.N) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(v[k]);
+                orow[col0 + k] = h;
+                if (lout) lout[col0 + k] = __float2bfloat16_rn(v[k] - __bfloat162float(h));
+              }
           }
         } else {
           // symmetric output: (row, c) for c >= row, and the mirror (c, row) for c > row
@@ -575,8 +605,8 @@ int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, 
   return launch<EPI_POLY, false>(ma, mb, p, kTracePoly, s);
 }
 
-int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, __nv_bfloat16 *Xn, int64_t batch, int64_t m, int64_t n,
-            float a, const float *s1, cudaStream_t s) {
+int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *Xn,
+            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, cudaStream_t s) {
   CUtensorMap ma, mb;
   int st = make_map(&ma, B, batch, m, m, BM);
   if (!st) st = make_map(&mb, X, batch, m, n, 64);
@@ -592,6 +622,8 @@ int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, __nv_bfloat16 *Xn, i
   p.src_mat = m * n;
   p.a = a;
   p.scale = s1;
+  p.src_lo = X_lo;
+  p.out_lo = Xn_lo;
   return launch<EPI_AXPY, true>(ma, mb, p, kTraceAxpy, s);
 }
 

@@ -58,9 +58,12 @@ def check_matrix(g, W_prev, b_prev, buf_new, u_in, O_gpu, W_new, rows, cols):
     sc = O.default_scale(rows, cols)
     exact = O.apply_update_fp32(W_prev, Og, LR, WD, sc)
     assert np.array_equal(bits16(W_new), O.bf16_bits(exact))
+    # fp64 chain: one bf16 ulp of the result plus what the update difference moves
     chain = O.apply_update(W_prev, want, LR, WD, sc)
-    ulp = np.abs(W_prev) * 2.0 ** -7 + 1e-30
-    assert np.all(np.abs(np32(W_new) - chain) <= ulp + LR * sc * np.abs(Og - want) + 1e-7)
+    Wn = np32(W_new)
+    mag = np.maximum(np.abs(Wn), np.abs(chain))
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(mag, 2.0 ** -126))) - 7)
+    assert np.all(np.abs(Wn - chain) <= ulp + LR * sc * np.abs(Og - want) * (1 + 1e-6) + 1e-12)
     return err
 
 

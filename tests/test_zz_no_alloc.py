@@ -36,8 +36,8 @@ def call_static(mk, X, steps=5):
 
 
 def test_static_scratch_matches_allocating_entry_point_twice(mk):
-    # one w2-shaped and one w1-shaped expert matrix: each needs about 57 MB of
-    # workspace, within the 64 MiB scratch; the second call follows the first
+    # one w2-shaped and one w1-shaped expert matrix: each needs about 79 MB of
+    # workspace, within the 96 MiB scratch; the second call follows the first
     shapes = [(1, workloads.EXPERT_HIDDEN, workloads.HIDDEN), (1, workloads.HIDDEN, workloads.EXPERT_HIDDEN)]
     assert all(mk.muon_ns_workspace_bytes(*s) <= mk.NS_STATIC_SCRATCH_BYTES for s in shapes)
     for k, (b, m, n) in enumerate(shapes):
