@@ -187,7 +187,8 @@ int copy_async(void *dst, const void *src, size_t bytes, cudaStream_t s) {
 // itself); with final_dst == nullptr it stays in whichever buffer the last
 // iteration wrote, returned through `result`.
 int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *final_dst, const Workspace &w, int64_t batch, int64_t mm,
-                 int64_t nn, int steps, const float *cf, float eps, cudaStream_t s, __nv_bfloat16 **result) {
+                 int64_t nn, bool transposed, int steps, const float *cf, float eps, cudaStream_t s,
+                 __nv_bfloat16 **result) {
   const int64_t per = mm * nn;
   MUON_TRY(launch_inv_norm_bf16(src0, batch, per, eps, w.partial, w.inv, w.inv2, s));
   auto *x1 = static_cast<__nv_bfloat16 *>(w.x1);
@@ -204,11 +205,11 @@ int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *final_dst, const Workspace 
     const bool last = it == steps - 1;
     __nv_bfloat16 *dst = (src == x1) ? x2 : x1;
     if (last && final_dst && final_dst != src) dst = final_dst;
-    MUON_TRY(ns_syrk(src, A, batch, mm, nn, it == 0 ? w.inv2 : nullptr, s));
+    MUON_TRY(ns_syrk(src, A, batch, mm, nn, it == 0 ? w.inv2 : nullptr, transposed, s));
     MUON_TRY(ns_poly(A, B, batch, mm, cf[1], cf[2], s));
     // the input X is exactly bf16 (no low half); the result leaves as bf16
     MUON_TRY(ns_axpy(B, src, it == 0 ? nullptr : lo, dst, last ? nullptr : lo, batch, mm, nn, cf[0],
-                     it == 0 ? w.inv : nullptr, s));
+                     it == 0 ? w.inv : nullptr, transposed, s));
     src = dst;
   }
   if (final_dst && src != final_dst) {
@@ -299,13 +300,9 @@ int muon_ns_batched_ws(void *X, int64_t batch, int64_t m, int64_t n, int steps, 
   Workspace w = carve(workspace, batch, mm, nn, 2);
   auto *x = static_cast<__nv_bfloat16 *>(X);
   __nv_bfloat16 *res = nullptr;
-  if (m <= n) return ns_bf16_core(x, x, w, batch, mm, nn, steps, cf, eps, s, &res);
-  // m > n: iterate on X^T (n x m) in the workspace and transpose the result
-  // back into X from whichever buffer the last iteration wrote.
-  auto *xt = static_cast<__nv_bfloat16 *>(w.x1);
-  MUON_TRY(launch_transpose_bf16(x, xt, batch, m, n, s));
-  MUON_TRY(ns_bf16_core(xt, nullptr, w, batch, mm, nn, steps, cf, eps, s, &res));
-  return launch_transpose_bf16(res, x, batch, mm, nn, s);
+  // m > n: the iteration runs on X^T without moving data -- the kernels read
+  // the stored matrix as the transpose of the canonical mm x nn one
+  return ns_bf16_core(x, x, w, batch, mm, nn, m > n, steps, cf, eps, s, &res);
 }
 
 int muon_ns_batched(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3], float eps,

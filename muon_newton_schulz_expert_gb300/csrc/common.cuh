@@ -68,18 +68,21 @@ int launch_scale_f32(const float *src, float *dst, int64_t batch, int64_t per, c
                      cudaStream_t s);
 
 // ---- tensor-core GEMMs of one Newton-Schulz iteration (gemm_tc.cu) ----
-// All matrices are batched, densely packed, bf16 row-major; X is m x n (m <= n).
+// All matrices are batched, densely packed, bf16 row-major; X is m x n (m <= n),
+// stored as m x n or, with `transposed`, as its transpose (n x m).
 // A = s2[b] * X X^T          (s2 == nullptr: 1), upper triangle computed, mirrored
 int ns_syrk(const __nv_bfloat16 *X, __nv_bfloat16 *A, int64_t batch, int64_t m, int64_t n, const float *s2,
-            cudaStream_t s);
+            bool transposed, cudaStream_t s);
 // B = b*A + c*A A            (A symmetric), upper triangle computed, mirrored
 int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, float b, float c,
             cudaStream_t s);
 // Xn = s1[b] * (a*X + B X)   (s1 == nullptr: 1), with X = X + X_lo and the
 // result split into Xn = bf16(result), Xn_lo = bf16(result - Xn); X_lo and
 // Xn_lo may be null (zero low half / not wanted) and may be the same buffer
+// (all of X, X_lo, Xn, Xn_lo in the same storage orientation)
 int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *Xn,
-            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, cudaStream_t s);
+            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, bool transposed,
+            cudaStream_t s);
 int selftest_wait(unsigned long long timeout_ns, cudaStream_t s);
 
 // ---- fp32 SIMT GEMMs for the verification mode (gemm_f32.cu) ----

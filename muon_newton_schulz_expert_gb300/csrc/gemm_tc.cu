@@ -48,15 +48,24 @@ constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + NUM_BARS * 8 + 16;
-constexpr int THREADS = 192;
+// AXPY epilogue staging: per epilogue warp one 32 x 32 bf16 box of X's high
+// half and one of its low half (64-byte swizzle), moved by TMA.
+constexpr int EPI_BOX = 32;
+constexpr int EPI_BOX_BYTES = EPI_BOX * EPI_BOX * 2;
+constexpr int EPI_BUF = 2 * EPI_BOX_BYTES;
+constexpr int EPI_WARPS_DECL = 8;
+constexpr int NUM_BARS = 2 * STAGES + 5 + EPI_WARPS_DECL;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS_DECL * EPI_BUF + 1024 + NUM_BARS * 8 + 16;
+constexpr int EPI_WARPS = EPI_WARPS_DECL;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer warp, MMA warp, 8 epilogue warps
 constexpr int ACC_COLS = BN;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 
 enum Epi { EPI_SYRK = 0, EPI_POLY = 1, EPI_AXPY = 2 };
 
 struct Params {
+  // AXPY epilogue maps (32 x 32 boxes): X high half, X low half, X' high, X' low
+  CUtensorMap tm_src, tm_src_lo, tm_out, tm_out_lo;
   int M, N, K;                 // output M x N, reduction length K (per matrix)
   int tiles_m, tiles_n;
   int tiles_per_mat;
@@ -143,6 +152,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory source of every committed store has been read
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every committed store has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// order this thread's generic-proxy shared-memory accesses before later async-proxy (TMA) accesses
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -186,11 +212,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, A K-major,
-// B K-major or MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(m >> 4) << 24);
+// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, each operand
+// K-major or MN-major (bits 15 and 16), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // Tile t -> (matrix, row tile, column tile).  Symmetric outputs enumerate, per
@@ -221,12 +247,57 @@ union Pack8 {
   __nv_bfloat162 h[4];
 };
 
-template <int EPI, bool B_MN>
+// Epilogue operands of one thread for one 32-column chunk of its row:
+// POLY: A (in hi); AXPY: X = hi + lo.  SYRK reads nothing.
+struct Chunk {
+  uint4 hi[4], lo[4];
+};
+
+template <int EPI>
+__device__ __forceinline__ void load_chunk(const Params &p, int mat, int row, int col0, Chunk &c) {
+  if (EPI == EPI_SYRK) return;
+  const bool valid = row < p.M && col0 < p.N;
+  const long long off = (long long)mat * p.src_mat + (long long)row * p.src_ld + col0;
+  const __nv_bfloat16 *srow = p.src + off;
+  const __nv_bfloat16 *lrow = (EPI == EPI_AXPY && p.src_lo) ? p.src_lo + off : nullptr;
+  if (valid && col0 + 32 <= p.N) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      c.hi[g] = __ldg(reinterpret_cast<const uint4 *>(srow) + g);
+      // plain load: the lo buffer is overwritten in place by this same thread later
+      c.lo[g] = lrow ? reinterpret_cast<const uint4 *>(lrow)[g] : make_uint4(0u, 0u, 0u, 0u);
+    }
+  } else {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      Pack8 th, tl;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k0 = g * 8 + 2 * e;
+        const bool ok0 = valid && col0 + k0 < p.N, ok1 = valid && col0 + k0 + 1 < p.N;
+        th.h[e] = __floats2bfloat162_rn(ok0 ? __bfloat162float(srow[k0]) : 0.f,
+                                        ok1 ? __bfloat162float(srow[k0 + 1]) : 0.f);
+        tl.h[e] = __floats2bfloat162_rn(ok0 && lrow ? __bfloat162float(lrow[k0]) : 0.f,
+                                        ok1 && lrow ? __bfloat162float(lrow[k0 + 1]) : 0.f);
+      }
+      c.hi[g] = th.v;
+      c.lo[g] = tl.v;
+    }
+  }
+}
+
+// One tile is 128 x 256; epilogue warp (2 + e) owns TMEM lane quadrant
+// warp % 4 (rows 32q..32q+31) and column half e / 4 (128 columns, 4 chunks).
+constexpr int CHUNKS = BN / 2 / 32;
+
+template <int EPI, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(THREADS, 1)
-    ns_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    ns_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint8_t *epi_smem = smem + STAGES * STAGE_BYTES;  // EPI_WARPS staging buffers, 1024-aligned
+  uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + EPI_WARPS * EPI_BUF);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -238,6 +309,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #define ACCF(a) (bar0 + 8u * (uint32_t)(2 * STAGES + (a)))
 #define ACCE(a) (bar0 + 8u * (uint32_t)(2 * STAGES + 2 + (a)))
   const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
+#define EBAR(e) (bar0 + 8u * (uint32_t)(2 * STAGES + 5 + (e)))
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -246,15 +318,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(ACCF(a), 1);
-      mbar_init(ACCE(a), 4 * 32);
+      mbar_init(ACCE(a), EPI_WARPS * 32);
     }
     mbar_init(drain_bar, 1);
+    for (int e = 0; e < EPI_WARPS; ++e) mbar_init(EBAR(e), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (EPI == EPI_AXPY) {
+      tma_prefetch_desc(&p.tm_src);
+      tma_prefetch_desc(&p.tm_out);
+    }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -285,12 +362,21 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           mbar_expect_tx(FULL(stage), STAGE_BYTES);
           const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_STAGE;
-          tma_load_3d(sa, &tmA, FULL(stage), kb * BK, ti * BM, mat);
+          // K-major operands: one box of rows x 64 K-columns.  MN-major operands:
+          // boxes of 64 M/N-columns x 64 K-rows, one per 64-wide swizzle atom.
+          if (!A_MN) {
+            tma_load_3d(sa, &tmA, FULL(stage), kb * BK, ti * BM, mat);
+          } else {
+#pragma unroll
+            for (int q = 0; q < BM / 64; ++q)
+              tma_load_3d(sa + q * (64 * BK * 2), &tmA, FULL(stage), ti * BM + q * 64, kb * BK, mat);
+          }
           if (!B_MN) {
             tma_load_3d(sb, &tmB, FULL(stage), kb * BK, tj * BN, mat);
           } else {
 #pragma unroll
-            for (int q = 0; q < BN / 64; ++q) tma_load_3d(sb + q * (64 * BK * 2), &tmB, FULL(stage), tj * BN + q * 64, kb * BK, mat);
+            for (int q = 0; q < BN / 64; ++q)
+              tma_load_3d(sb + q * (64 * BK * 2), &tmB, FULL(stage), tj * BN + q * 64, kb * BK, mat);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -303,7 +389,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(BM, BN, B_MN);
+      constexpr uint32_t idesc = make_idesc(BM, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -322,7 +408,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_STAGE;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            const uint64_t adesc = smem_desc(sa + kk * (UMMA_K * 2), 16, 1024);
+            // K-major: advance 16 K-elements (32 bytes) inside the swizzle row.
+            // MN-major: advance 16 K-rows (two 8-row groups of 1024 bytes);
+            // LBO = 8192 bytes between 64-wide atoms, SBO = 1024 between K groups.
+            const uint64_t adesc = A_MN ? smem_desc(sa + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
+                                        : smem_desc(sa + kk * (UMMA_K * 2), 16, 1024);
             const uint64_t bdesc = B_MN ? smem_desc(sb + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
                                         : smem_desc(sb + kk * (UMMA_K * 2), 16, 1024);
             tc_mma(d, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
@@ -340,139 +430,233 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // all MMAs issued by this thread have completed once drain_bar flips
       tc_commit(drain_bar);
-      Watch wd{abort_flag, p.err, p.timeout_ns};
       volatile int no_abort = 0;
-      wd.abort = &no_abort;
-      wait_bounded(drain_bar, 0, wd);
+      wait_bounded(drain_bar, 0, Watch{&no_abort, p.err, p.timeout_ns});
     }
-  } else {
-    // ---------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quadrant accessible to this warp
+  } else if (EPI == EPI_AXPY) {
+    // ---------------------------------------------------------------- AXPY epilogue
+    // X' = s (a (hi + lo) + acc) through shared memory: each warp stages a
+    // 32 x 32 box of hi and of lo (TMA load, zero-filled past the edges),
+    // overwrites it with hi' = bf16(X'), lo' = bf16(X' - hi') and TMA-stores
+    // it (clipped at the edges).  Lane i owns row i of the box, which is TMEM
+    // lane 32q + i; the 64-byte swizzle makes these row reads conflict-free.
+    const int ew = warp - 2;
+    const int q = warp & 3, half = ew >> 2;
+    uint8_t *ebuf = epi_smem + ew * EPI_BUF;   // [hi box][lo box]
+    const uint32_t ebuf_s = smem_u32(ebuf);
+    const uint32_t ebar = EBAR(ew);
+    uint32_t ephase = 0;
+    const bool lo_in = p.src_lo != nullptr, lo_out = p.out_lo != nullptr;
+    const uint32_t etx = lo_in ? 2u * EPI_BOX_BYTES : (uint32_t)EPI_BOX_BYTES;
+    auto epi_load = [&](int m_, int row0_, int col0_) {  // lane 0 only
+      fence_proxy_async_smem();
+      mbar_expect_tx(ebar, etx);
+      tma_load_3d(ebuf_s, &p.tm_src, ebar, col0_, row0_, m_);
+      if (lo_in) tma_load_3d(ebuf_s + EPI_BOX_BYTES, &p.tm_src_lo, ebar, col0_, row0_, m_);
+    };
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (long long t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      int mat, ti, tj;
+    long long t = blockIdx.x;
+    int mat = 0, ti = 0, tj = 0;
+    if (t < p.num_tiles) {
       decode_tile<EPI>(p, t, mat, ti, tj);
+      if (lane == 0) epi_load(mat, ti * BM + q * 32, tj * BN + half * 128);
+    }
+    bool alive = true;
+    for (; alive && t < p.num_tiles; t += gridDim.x) {
+      const long long tn = t + gridDim.x;
+      int mat_n = 0, ti_n = 0, tj_n = 0;
+      if (tn < p.num_tiles) decode_tile<EPI>(p, tn, mat_n, ti_n, tj_n);
+      const bool ok = wait_bounded(ACCF(acc), acc_phase, w);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int row0 = ti * BM + q * 32;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS + half * 128);
+      const float sc = p.scale ? p.scale[mat] : 1.0f;
+#pragma unroll 1
+      for (int ch = 0; ch < CHUNKS; ++ch) {
+        const int col0 = tj * BN + half * 128 + ch * 32;
+        const bool got = wait_bounded(ebar, ephase, w);
+        if (!__all_sync(0xffffffffu, got)) {
+          alive = false;
+          break;
+        }
+        ephase ^= 1u;
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(taddr + (uint32_t)(ch * 32), r);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t off = (uint32_t)(lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
+          Pack8 hv, lv, ho, lo;
+          hv.v = *reinterpret_cast<const uint4 *>(ebuf + off);
+          lv.v = lo_in ? *reinterpret_cast<const uint4 *>(ebuf + EPI_BOX_BYTES + off) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k = c * 8 + 2 * e;
+            const float2 fh = __bfloat1622float2(hv.h[e]), fl = __bfloat1622float2(lv.h[e]);
+            const float v0 = sc * fmaf(p.a, fh.x + fl.x, __uint_as_float(r[k]));
+            const float v1 = sc * fmaf(p.a, fh.y + fl.y, __uint_as_float(r[k + 1]));
+            ho.h[e] = __floats2bfloat162_rn(v0, v1);
+            const float2 hh = __bfloat1622float2(ho.h[e]);
+            lo.h[e] = __floats2bfloat162_rn(v0 - hh.x, v1 - hh.y);
+          }
+          *reinterpret_cast<uint4 *>(ebuf + off) = ho.v;
+          if (lo_out) *reinterpret_cast<uint4 *>(ebuf + EPI_BOX_BYTES + off) = lo.v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&p.tm_out, ebuf_s, col0, row0, mat);
+          if (lo_out) tma_store_3d(&p.tm_out_lo, ebuf_s + EPI_BOX_BYTES, col0, row0, mat);
+          bulk_commit();
+          bulk_wait_read_all();
+          // the staging box is free again: fetch the next chunk's operands
+          if (ch + 1 < CHUNKS)
+            epi_load(mat, row0, col0 + 32);
+          else if (tn < p.num_tiles)
+            epi_load(mat_n, ti_n * BM + q * 32, tj_n * BN + half * 128);
+        }
+        __syncwarp();
+      }
+      if (!alive) break;
+      tc_fence_before();
+      mbar_arrive(ACCE(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+      mat = mat_n;
+      ti = ti_n;
+      tj = tj_n;
+    }
+    if (lane == 0) bulk_wait_all();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;            // TMEM lane quadrant accessible to this warp
+    const int half = (warp - 2) >> 2;  // which 128 columns of the tile
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    long long t = blockIdx.x;
+    int mat = 0, ti = 0, tj = 0;
+    Chunk cur, nxt;
+    if (t < p.num_tiles) {
+      decode_tile<EPI>(p, t, mat, ti, tj);
+      load_chunk<EPI>(p, mat, ti * BM + q * 32 + lane, tj * BN + half * 128, cur);
+    }
+    for (; t < p.num_tiles; t += gridDim.x) {
+      const long long tn = t + gridDim.x;
+      int mat_n = 0, ti_n = 0, tj_n = 0;
+      if (tn < p.num_tiles) decode_tile<EPI>(p, tn, mat_n, ti_n, tj_n);
       const bool ok = wait_bounded(ACCF(acc), acc_phase, w);
       if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: the TMEM loads below are .sync.aligned
       tc_fence_after();
       const int row = ti * BM + q * 32 + lane;
       const bool row_ok = row < p.M;
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS + half * 128);
       const float sc = p.scale ? p.scale[mat] : 1.0f;
       __nv_bfloat16 *outm = p.out + (long long)mat * p.out_mat;
-      const __nv_bfloat16 *srcm = p.src ? p.src + (long long)mat * p.src_mat : nullptr;
 #pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
+      for (int ch = 0; ch < CHUNKS; ++ch) {
+        const int col0 = tj * BN + half * 128 + ch * 32;
+        // prefetch the operands of the next chunk (or of the next tile's first chunk)
+        if (ch + 1 < CHUNKS)
+          load_chunk<EPI>(p, mat, row, col0 + 32, nxt);
+        else if (tn < p.num_tiles)
+          load_chunk<EPI>(p, mat_n, ti_n * BM + q * 32 + lane, tj_n * BN + half * 128, nxt);
         uint32_t r[32];
         __syncwarp();
         tmem_ld32(taddr + (uint32_t)(ch * 32), r);
-        const int col0 = tj * BN + ch * 32;
-        if (!row_ok || col0 >= p.N) continue;
-        float v[32];
-        if (EPI == EPI_SYRK) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = sc * __uint_as_float(r[k]);
-        } else {
-          // a*X + acc (AXPY, X = hi + lo) or b*A + c*acc (POLY), reading the epilogue operand row
-          const long long eoff = (long long)row * p.src_ld + col0;
-          const __nv_bfloat16 *srow = srcm + eoff;
-          const __nv_bfloat16 *lrow =
-              (EPI == EPI_AXPY && p.src_lo) ? p.src_lo + (long long)mat * p.src_mat + eoff : nullptr;
-          const bool full_chunk = col0 + 32 <= p.N;
+        if (row_ok && col0 < p.N) {
+          float v[32];
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            Pack8 s8, l8;
-            if (full_chunk) {
-              s8.v = __ldg(reinterpret_cast<const uint4 *>(srow) + g);
-              // plain load: the lo buffer may be the one this thread overwrites below
-              l8.v = lrow ? reinterpret_cast<const uint4 *>(lrow)[g] : make_uint4(0u, 0u, 0u, 0u);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int k0 = g * 8 + 2 * e;
-                const bool ok0 = col0 + k0 < p.N, ok1 = col0 + k0 + 1 < p.N;
-                s8.h[e] = __floats2bfloat162_rn(ok0 ? __bfloat162float(srow[k0]) : 0.f,
-                                                ok1 ? __bfloat162float(srow[k0 + 1]) : 0.f);
-                l8.h[e] = __floats2bfloat162_rn(ok0 && lrow ? __bfloat162float(lrow[k0]) : 0.f,
-                                                ok1 && lrow ? __bfloat162float(lrow[k0 + 1]) : 0.f);
-              }
-            }
+            Pack8 ch_hi, ch_lo;
+            ch_hi.v = cur.hi[g];
+            ch_lo.v = cur.lo[g];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              float2 f = __bfloat1622float2(s8.h[e]);
               const int k = g * 8 + 2 * e;
-              if (EPI == EPI_AXPY) {
-                const float2 fl = __bfloat1622float2(l8.h[e]);
-                v[k] = sc * fmaf(p.a, f.x + fl.x, __uint_as_float(r[k]));
-                v[k + 1] = sc * fmaf(p.a, f.y + fl.y, __uint_as_float(r[k + 1]));
+              const float a0 = __uint_as_float(r[k]), a1 = __uint_as_float(r[k + 1]);
+              if (EPI == EPI_SYRK) {
+                v[k] = sc * a0;
+                v[k + 1] = sc * a1;
+              } else if (EPI == EPI_POLY) {
+                const float2 f = __bfloat1622float2(ch_hi.h[e]);
+                v[k] = fmaf(p.c, a0, p.b * f.x);
+                v[k + 1] = fmaf(p.c, a1, p.b * f.y);
               } else {
-                v[k] = fmaf(p.c, __uint_as_float(r[k]), p.b * f.x);
-                v[k + 1] = fmaf(p.c, __uint_as_float(r[k + 1]), p.b * f.y);
+                const float2 f = __bfloat1622float2(ch_hi.h[e]), fl = __bfloat1622float2(ch_lo.h[e]);
+                v[k] = sc * fmaf(p.a, f.x + fl.x, a0);
+                v[k + 1] = sc * fmaf(p.a, f.y + fl.y, a1);
               }
             }
           }
-        }
-        __nv_bfloat16 *orow = outm + (long long)row * p.out_ld;
-        if (EPI == EPI_AXPY) {
-          __nv_bfloat16 *lout = p.out_lo ? p.out_lo + (long long)mat * p.out_mat + (long long)row * p.out_ld : nullptr;
-          if (col0 + 32 <= p.N) {
+          __nv_bfloat16 *orow = outm + (long long)row * p.out_ld;
+          if (EPI == EPI_AXPY) {
+            __nv_bfloat16 *lout =
+                p.out_lo ? p.out_lo + (long long)mat * p.out_mat + (long long)row * p.out_ld : nullptr;
+            if (col0 + 32 <= p.N) {
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              Pack8 o, ol;
+              for (int g = 0; g < 4; ++g) {
+                Pack8 o, ol;
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int k = g * 8 + 2 * e;
-                o.h[e] = __floats2bfloat162_rn(v[k], v[k + 1]);
-                const float2 h = __bfloat1622float2(o.h[e]);
-                ol.h[e] = __floats2bfloat162_rn(v[k] - h.x, v[k + 1] - h.y);
+                for (int e = 0; e < 4; ++e) {
+                  const int k = g * 8 + 2 * e;
+                  o.h[e] = __floats2bfloat162_rn(v[k], v[k + 1]);
+                  const float2 hh = __bfloat1622float2(o.h[e]);
+                  ol.h[e] = __floats2bfloat162_rn(v[k] - hh.x, v[k + 1] - hh.y);
+                }
+                reinterpret_cast<uint4 *>(orow + col0)[g] = o.v;
+                if (lout) reinterpret_cast<uint4 *>(lout + col0)[g] = ol.v;
               }
-              reinterpret_cast<uint4 *>(orow + col0)[g] = o.v;
-              if (lout) reinterpret_cast<uint4 *>(lout + col0)[g] = ol.v;
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                if (col0 + k < p.N) {
+                  const __nv_bfloat16 hh = __float2bfloat16_rn(v[k]);
+                  orow[col0 + k] = hh;
+                  if (lout) lout[col0 + k] = __float2bfloat16_rn(v[k] - __bfloat162float(hh));
+                }
             }
           } else {
+            // symmetric output: (row, c) for c >= row, and the mirror (c, row) for c > row
+            if (col0 >= row && col0 + 32 <= p.N) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k)
-              if (col0 + k < p.N) {
-                const __nv_bfloat16 h = __float2bfloat16_rn(v[k]);
-                orow[col0 + k] = h;
-                if (lout) lout[col0 + k] = __float2bfloat16_rn(v[k] - __bfloat162float(h));
+              for (int g = 0; g < 4; ++g) {
+                Pack8 o;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o.h[e] = __floats2bfloat162_rn(v[g * 8 + 2 * e], v[g * 8 + 2 * e + 1]);
+                reinterpret_cast<uint4 *>(orow + col0)[g] = o.v;
               }
-          }
-        } else {
-          // symmetric output: (row, c) for c >= row, and the mirror (c, row) for c > row
-          if (col0 >= row && col0 + 32 <= p.N) {
+            } else {
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              Pack8 o;
-#pragma unroll
-              for (int e = 0; e < 4; ++e) o.h[e] = __floats2bfloat162_rn(v[g * 8 + 2 * e], v[g * 8 + 2 * e + 1]);
-              reinterpret_cast<uint4 *>(orow + col0)[g] = o.v;
+              for (int k = 0; k < 32; ++k) {
+                const int c = col0 + k;
+                if (c >= row && c < p.N) orow[c] = __float2bfloat16_rn(v[k]);
+              }
             }
-          } else {
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
               const int c = col0 + k;
-              if (c >= row && c < p.N) orow[c] = __float2bfloat16_rn(v[k]);
+              if (c > row && c < p.N) outm[(long long)c * p.out_ld + row] = __float2bfloat16_rn(v[k]);
             }
           }
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int c = col0 + k;
-            if (c > row && c < p.N) outm[(long long)c * p.out_ld + row] = __float2bfloat16_rn(v[k]);
-          }
         }
+        cur = nxt;
       }
       tc_fence_before();
       mbar_arrive(ACCE(acc));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
+      mat = mat_n;
+      ti = ti_n;
+      tj = tj_n;
     }
   }
 #undef FULL
 #undef EMPTY
 #undef ACCF
 #undef ACCE
+#undef EBAR
 
   tc_fence_before();
   __syncthreads();
@@ -518,21 +702,22 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D map over a dense [batch][rows][cols] bf16 stack; box = 64 columns x box_rows rows x 1 matrix.
-int make_map(CUtensorMap *map, const void *base, int64_t batch, int64_t rows, int64_t cols, int box_rows) {
+// 3-D map over a dense [batch][rows][cols] bf16 stack; box = box_cols columns x box_rows rows x 1 matrix.
+int make_map(CUtensorMap *map, const void *base, int64_t batch, int64_t rows, int64_t cols, int box_rows,
+             int box_cols = 64, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return MUON_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
   cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(rows * cols * 2)};
-  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MUON_OK : MUON_ERR_CUDA;
 }
 
-template <int EPI, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN>
 int launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int trace_kind, cudaStream_t s) {
   if (p.num_tiles == 0) return MUON_OK;
   static std::once_flag attr_once[64];
@@ -540,12 +725,13 @@ int launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int tr
   if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
   cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once[dev & 63], [&] {
-    attr_err = cudaFuncSetAttribute(ns_gemm_kernel<EPI, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr_err =
+        cudaFuncSetAttribute(ns_gemm_kernel<EPI, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return MUON_ERR_CUDA;
   const long long grid = std::min<long long>(p.num_tiles, num_sms());
   trace_before(trace_kind, s);
-  ns_gemm_kernel<EPI, B_MN><<<(unsigned)grid, THREADS, SMEM_BYTES, s>>>(ma, mb, p);
+  ns_gemm_kernel<EPI, A_MN, B_MN><<<(unsigned)grid, THREADS, SMEM_BYTES, s>>>(ma, mb, p);
   return trace_after(trace_kind, s);
 }
 
@@ -571,10 +757,16 @@ int triangle_tiles(int tiles_m, int tiles_n) {
 }  // namespace
 
 int ns_syrk(const __nv_bfloat16 *X, __nv_bfloat16 *A, int64_t batch, int64_t m, int64_t n, const float *s2,
-            cudaStream_t s) {
+            bool transposed, cudaStream_t s) {
   CUtensorMap ma, mb;
-  int st = make_map(&ma, X, batch, m, n, BM);
-  if (!st) st = make_map(&mb, X, batch, m, n, BN);
+  int st;
+  if (!transposed) {  // X stored m x n: both operands K-major
+    st = make_map(&ma, X, batch, m, n, BM);
+    if (!st) st = make_map(&mb, X, batch, m, n, BN);
+  } else {            // X stored n x m (X^T): both operands MN-major, 64 x 64 boxes
+    st = make_map(&ma, X, batch, n, m, 64);
+    mb = ma;
+  }
   if (st) return st;
   Params p = base_params((int)m, (int)m, (int)n, batch);
   p.tiles_per_mat = triangle_tiles(p.tiles_m, p.tiles_n);
@@ -583,7 +775,8 @@ int ns_syrk(const __nv_bfloat16 *X, __nv_bfloat16 *A, int64_t batch, int64_t m, 
   p.out_ld = m;
   p.out_mat = m * m;
   p.scale = s2;
-  return launch<EPI_SYRK, false>(ma, mb, p, kTraceSyrk, s);
+  return transposed ? launch<EPI_SYRK, true, true>(ma, mb, p, kTraceSyrk, s)
+                    : launch<EPI_SYRK, false, false>(ma, mb, p, kTraceSyrk, s);
 }
 
 int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, float b, float c, cudaStream_t s) {
@@ -602,29 +795,50 @@ int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, 
   p.src_mat = m * m;
   p.b = b;
   p.c = c;
-  return launch<EPI_POLY, false>(ma, mb, p, kTracePoly, s);
+  return launch<EPI_POLY, false, false>(ma, mb, p, kTracePoly, s);
 }
 
 int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *Xn,
-            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, cudaStream_t s) {
+            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, bool transposed,
+            cudaStream_t s) {
   CUtensorMap ma, mb;
-  int st = make_map(&ma, B, batch, m, m, BM);
-  if (!st) st = make_map(&mb, X, batch, m, n, 64);
+  int st;
+  Params p;
+  if (!transposed) {
+    // X' (m x n) = a X + B X: A operand B (K-major), B operand X (MN-major)
+    st = make_map(&ma, B, batch, m, m, BM);
+    if (!st) st = make_map(&mb, X, batch, m, n, 64);
+    p = base_params((int)m, (int)n, (int)m, batch);
+    p.out_ld = n;
+  } else {
+    // X stored n x m: X'^T = a X^T + X^T B (B symmetric), both operands K-major
+    st = make_map(&ma, X, batch, n, m, BM);
+    if (!st) st = make_map(&mb, B, batch, m, m, BN);
+    p = base_params((int)n, (int)m, (int)m, batch);
+    p.out_ld = m;
+  }
   if (st) return st;
-  Params p = base_params((int)m, (int)n, (int)m, batch);
+  // epilogue boxes over X, X_lo, Xn, Xn_lo, all stored p.M x p.N
+  const int eb = EPI_BOX;
+  const CUtensorMapSwizzle sw64 = CU_TENSOR_MAP_SWIZZLE_64B;
+  st = make_map(&p.tm_src, X, batch, p.M, p.N, eb, eb, sw64);
+  if (!st && X_lo) st = make_map(&p.tm_src_lo, X_lo, batch, p.M, p.N, eb, eb, sw64);
+  if (!st) st = make_map(&p.tm_out, Xn, batch, p.M, p.N, eb, eb, sw64);
+  if (!st && Xn_lo) st = make_map(&p.tm_out_lo, Xn_lo, batch, p.M, p.N, eb, eb, sw64);
+  if (st) return st;
   p.tiles_per_mat = p.tiles_m * p.tiles_n;
   p.num_tiles = (long long)p.tiles_per_mat * batch;
   p.out = Xn;
-  p.out_ld = n;
   p.out_mat = m * n;
   p.src = X;
-  p.src_ld = n;
+  p.src_ld = p.out_ld;
   p.src_mat = m * n;
   p.a = a;
   p.scale = s1;
   p.src_lo = X_lo;
   p.out_lo = Xn_lo;
-  return launch<EPI_AXPY, true>(ma, mb, p, kTraceAxpy, s);
+  return transposed ? launch<EPI_AXPY, false, false>(ma, mb, p, kTraceAxpy, s)
+                    : launch<EPI_AXPY, false, true>(ma, mb, p, kTraceAxpy, s);
 }
 
 int selftest_wait(unsigned long long timeout_ns, cudaStream_t s) {
