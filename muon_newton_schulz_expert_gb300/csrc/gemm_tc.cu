@@ -17,20 +17,26 @@
 // on rank-deficient or ill-conditioned inputs that noise grows to ~10% of the
 // output; with the lo half it stays near 2^-17.
 //
-// Design (one persistent CTA per SM, 192 threads, warp-specialised):
-//   warp 0 lane 0  TMA producer: 128x64 and 256x64 bf16 tiles with 128-byte
-//                  swizzle into a 4-stage shared-memory ring (mbarrier
-//                  complete_tx);
-//   warp 1         TMEM allocation (512 columns = two 128x256 fp32
-//                  accumulators); lane 0 issues tcgen05.mma (M=128, N=256,
-//                  K=16, bf16 in, fp32 accumulate) and tcgen05.commit;
-//   warps 2..5     epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//                  lanes 32*(w%4)..+31), fp32 epilogue math, bf16 stores.
+// Design: persistent CTA pairs (clusters of 2), one CTA per SM, 320 threads,
+// warp-specialised.  A pair computes a 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M=256, N=256, K=16, bf16 in, fp32 accumulate):
+// each CTA holds 128 rows of A and a 128-row half of B in its own shared
+// memory, and each CTA's TMEM receives its 128 rows of the accumulator.  Per
+// SM this reads half the B bytes of a single-CTA 128 x 256 tile, which is what
+// keeps shared-memory bandwidth below the tensor cores' appetite.
+//   warp 0 lane 0  TMA producer (both CTAs): 128x64 bf16 boxes, 128-byte
+//                  swizzle, 6-stage ring; completion is signalled on the even
+//                  CTA's "full" barrier, which waits for both halves;
+//   warp 1         TMEM allocation of 512 columns (two 128 x 256 fp32
+//                  accumulators) in both CTAs; lane 0 of the even CTA issues
+//                  the MMAs and multicasts tcgen05.commit to both CTAs;
+//   warps 2..9     epilogue (both CTAs): warp w reads TMEM lanes
+//                  32*(w%4)..+31 and one 128-column half of the tile.
 // The double-buffered accumulator lets the epilogue of tile t overlap the
 // main loop of tile t+1.  Every mbarrier wait is bounded: when it runs out the
 // kernel records a timeout in the device error word, raises a shared abort
 // flag so the other roles stop, lets in-flight copies land, frees its TMEM and
-// returns.  No cluster multicast is used: each CTA loads its own tiles.
+// returns.  No TMA multicast is used: each CTA loads its own tiles.
 #include <cuda.h>
 
 #include <mutex>
@@ -40,26 +46,28 @@
 namespace muon {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+constexpr int CM = 256;    // rows of a pair tile
+constexpr int BM = 128;    // rows of a pair tile held by one CTA
+constexpr int BN = 256;    // columns of a pair tile
+constexpr int BNH = 128;   // rows of the B operand held by one CTA
+constexpr int BK = 64;     // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
-constexpr int A_STAGE = BM * BK * 2;  // 16 KB
-constexpr int B_STAGE = BN * BK * 2;  // 32 KB
+constexpr int STAGES = 6;
+constexpr int A_STAGE = BM * BK * 2;   // 16 KB
+constexpr int B_STAGE = BNH * BK * 2;  // 16 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 // AXPY epilogue staging: per epilogue warp one 32 x 32 bf16 box of X's high
 // half and one of its low half (64-byte swizzle), moved by TMA.
 constexpr int EPI_BOX = 32;
 constexpr int EPI_BOX_BYTES = EPI_BOX * EPI_BOX * 2;
 constexpr int EPI_BUF = 2 * EPI_BOX_BYTES;
-constexpr int EPI_WARPS_DECL = 8;
-constexpr int NUM_BARS = 2 * STAGES + 5 + EPI_WARPS_DECL;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS_DECL * EPI_BUF + 1024 + NUM_BARS * 8 + 16;
-constexpr int EPI_WARPS = EPI_WARPS_DECL;
+constexpr int EPI_WARPS = 8;
+constexpr int NUM_BARS = 2 * STAGES + 5 + EPI_WARPS;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF + 1024 + NUM_BARS * 8 + 16;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer warp, MMA warp, 8 epilogue warps
 constexpr int ACC_COLS = BN;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
+constexpr int CHUNKS = BN / 2 / 32;  // 32-column chunks per epilogue thread and tile
 
 enum Epi { EPI_SYRK = 0, EPI_POLY = 1, EPI_AXPY = 2 };
 
@@ -67,7 +75,7 @@ struct Params {
   // AXPY epilogue maps (32 x 32 boxes): X high half, X low half, X' high, X' low
   CUtensorMap tm_src, tm_src_lo, tm_out, tm_out_lo;
   int M, N, K;                 // output M x N, reduction length K (per matrix)
-  int tiles_m, tiles_n;
+  int tiles_m, tiles_n;        // pair tiles of 256 x 256
   int tiles_per_mat;
   long long num_tiles;
   __nv_bfloat16 *out;
@@ -95,10 +103,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -152,6 +156,43 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// Pair form: the completion is signalled on an mbarrier that may live in the
+// peer CTA (a shared::cluster address), here always the pair's even CTA.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                                 int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (possibly in the
+// peer CTA), with the default release semantics of mbarrier.arrive.  A
+// cluster-scope release here would make every arrival wait for this thread's
+// earlier global stores to drain.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// every thread of both CTAs of the cluster
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
@@ -176,8 +217,13 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+// Arrives once on the mbarrier at offset `bar` in every CTA of the pair named
+// in `mask` when all MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
+               : "memory");
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -185,7 +231,7 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -219,9 +265,9 @@ __host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool a_mn_major,
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-// Tile t -> (matrix, row tile, column tile).  Symmetric outputs enumerate, per
-// matrix, the tiles that hold at least one element on or above the diagonal:
-// row tile i covers rows [128i, 128i+128) and needs column tiles j >= i/2.
+// Tile t -> (matrix, row tile, column tile) of 256 x 256 pair tiles.
+// Symmetric outputs enumerate, per matrix, the tiles on or above the
+// diagonal: row tile i needs column tiles j >= i.
 template <int EPI>
 __device__ __forceinline__ void decode_tile(const Params &p, long long t, int &mat, int &ti, int &tj) {
   mat = (int)(t / p.tiles_per_mat);
@@ -232,13 +278,13 @@ __device__ __forceinline__ void decode_tile(const Params &p, long long t, int &m
   } else {
     int i = 0;
     for (;;) {
-      int cnt = p.tiles_n - (i >> 1);
+      const int cnt = p.tiles_n - i;
       if (r < cnt) break;
       r -= cnt;
       ++i;
     }
     ti = i;
-    tj = (i >> 1) + r;
+    tj = i + r;
   }
 }
 
@@ -247,48 +293,35 @@ union Pack8 {
   __nv_bfloat162 h[4];
 };
 
-// Epilogue operands of one thread for one 32-column chunk of its row:
-// POLY: A (in hi); AXPY: X = hi + lo.  SYRK reads nothing.
+// Epilogue operands of one thread for one 32-column chunk of its row
+// (POLY: A in hi).  AXPY stages its operands through shared memory instead.
 struct Chunk {
-  uint4 hi[4], lo[4];
+  uint4 hi[4];
 };
 
 template <int EPI>
 __device__ __forceinline__ void load_chunk(const Params &p, int mat, int row, int col0, Chunk &c) {
-  if (EPI == EPI_SYRK) return;
+  if (EPI != EPI_POLY) return;
   const bool valid = row < p.M && col0 < p.N;
-  const long long off = (long long)mat * p.src_mat + (long long)row * p.src_ld + col0;
-  const __nv_bfloat16 *srow = p.src + off;
-  const __nv_bfloat16 *lrow = (EPI == EPI_AXPY && p.src_lo) ? p.src_lo + off : nullptr;
+  const __nv_bfloat16 *srow = p.src + (long long)mat * p.src_mat + (long long)row * p.src_ld + col0;
   if (valid && col0 + 32 <= p.N) {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      c.hi[g] = __ldg(reinterpret_cast<const uint4 *>(srow) + g);
-      // plain load: the lo buffer is overwritten in place by this same thread later
-      c.lo[g] = lrow ? reinterpret_cast<const uint4 *>(lrow)[g] : make_uint4(0u, 0u, 0u, 0u);
-    }
+    for (int g = 0; g < 4; ++g) c.hi[g] = __ldg(reinterpret_cast<const uint4 *>(srow) + g);
   } else {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      Pack8 th, tl;
+      Pack8 th;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int k0 = g * 8 + 2 * e;
         const bool ok0 = valid && col0 + k0 < p.N, ok1 = valid && col0 + k0 + 1 < p.N;
         th.h[e] = __floats2bfloat162_rn(ok0 ? __bfloat162float(srow[k0]) : 0.f,
                                         ok1 ? __bfloat162float(srow[k0 + 1]) : 0.f);
-        tl.h[e] = __floats2bfloat162_rn(ok0 && lrow ? __bfloat162float(lrow[k0]) : 0.f,
-                                        ok1 && lrow ? __bfloat162float(lrow[k0 + 1]) : 0.f);
       }
       c.hi[g] = th.v;
-      c.lo[g] = tl.v;
     }
   }
 }
-
-// One tile is 128 x 256; epilogue warp (2 + e) owns TMEM lane quadrant
-// warp % 4 (rows 32q..32q+31) and column half e / 4 (128 columns, 4 chunks).
-constexpr int CHUNKS = BN / 2 / 32;
 
 template <int EPI, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -304,21 +337,23 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();          // 0: issues the MMAs; 1: its peer
+  const long long cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 #define FULL(s) (bar0 + 8u * (uint32_t)(s))
 #define EMPTY(s) (bar0 + 8u * (uint32_t)(STAGES + (s)))
 #define ACCF(a) (bar0 + 8u * (uint32_t)(2 * STAGES + (a)))
 #define ACCE(a) (bar0 + 8u * (uint32_t)(2 * STAGES + 2 + (a)))
-  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
 #define EBAR(e) (bar0 + 8u * (uint32_t)(2 * STAGES + 5 + (e)))
+  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(FULL(s), 1);
-      mbar_init(EMPTY(s), 1);
+      mbar_init(FULL(s), 1);    // used in CTA 0: its producer's expect_tx for both halves
+      mbar_init(EMPTY(s), 1);   // multicast commit
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(ACCF(a), 1);
-      mbar_init(ACCE(a), EPI_WARPS * 32);
+      mbar_init(ACCF(a), 1);                 // multicast commit
+      mbar_init(ACCE(a), 2 * EPI_WARPS);     // used in CTA 0: every epilogue warp of the pair
     }
     mbar_init(drain_bar, 1);
     for (int e = 0; e < EPI_WARPS; ++e) mbar_init(EBAR(e), 1);
@@ -333,50 +368,57 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_prefetch_desc(&p.tm_out);
     }
   }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+  if (warp == 1) {  // one warp in each CTA of the pair allocates the same columns in both
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(TMEM_COLS)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // the peer's barriers are initialised before anyone signals them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Watch w{abort_flag, p.err, p.timeout_ns};
   const int num_kb = (p.K + BK - 1) / BK;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer
+    // ---------------------------------------------------------------- producer (both CTAs)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (long long t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      for (long long t = cid; t < p.num_tiles; t += ncl) {
         int mat, ti, tj;
         decode_tile<EPI>(p, t, mat, ti, tj);
+        const int arow = ti * CM + (int)rank * BM;    // this CTA's rows of A
+        const int brow = tj * BN + (int)rank * BNH;   // this CTA's half of B
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(EMPTY(stage), phase ^ 1u, w)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(FULL(stage), STAGE_BYTES);
+          // CTA 0's barrier counts the bytes of both halves; CTA 1's loads only
+          // complete bytes on it (a stage is refilled only after the MMAs that
+          // read it finished, so no load can run ahead into the next phase)
+          const uint32_t full0 = map_to_rank(FULL(stage), 0);
+          if (rank == 0) mbar_expect_tx(FULL(stage), 2 * STAGE_BYTES);
           const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_STAGE;
-          // K-major operands: one box of rows x 64 K-columns.  MN-major operands:
-          // boxes of 64 M/N-columns x 64 K-rows, one per 64-wide swizzle atom.
+          // K-major operands: one box of 128 rows x 64 K-columns.  MN-major
+          // operands: boxes of 64 M/N-columns x 64 K-rows, one per swizzle atom.
           if (!A_MN) {
-            tma_load_3d(sa, &tmA, FULL(stage), kb * BK, ti * BM, mat);
+            tma_load_3d_pair(sa, &tmA, full0, kb * BK, arow, mat);
           } else {
 #pragma unroll
             for (int q = 0; q < BM / 64; ++q)
-              tma_load_3d(sa + q * (64 * BK * 2), &tmA, FULL(stage), ti * BM + q * 64, kb * BK, mat);
+              tma_load_3d_pair(sa + q * (64 * BK * 2), &tmA, full0, arow + q * 64, kb * BK, mat);
           }
           if (!B_MN) {
-            tma_load_3d(sb, &tmB, FULL(stage), kb * BK, tj * BN, mat);
+            tma_load_3d_pair(sb, &tmB, full0, kb * BK, brow, mat);
           } else {
 #pragma unroll
-            for (int q = 0; q < BN / 64; ++q)
-              tma_load_3d(sb + q * (64 * BK * 2), &tmB, FULL(stage), tj * BN + q * 64, kb * BK, mat);
+            for (int q = 0; q < BNH / 64; ++q)
+              tma_load_3d_pair(sb + q * (64 * BK * 2), &tmB, full0, brow + q * 64, kb * BK, mat);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -387,14 +429,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(BM, BN, A_MN, B_MN);
+    // ---------------------------------------------------------------- MMA issuer (CTA 0 of the pair)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = make_idesc(CM, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (long long t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      for (long long t = cid; t < p.num_tiles; t += ncl) {
         if (!wait_bounded(ACCE(acc), acc_phase ^ 1u, w)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * ACC_COLS);
@@ -411,30 +453,31 @@ __global__ void __launch_bounds__(THREADS, 1)
             // K-major: advance 16 K-elements (32 bytes) inside the swizzle row.
             // MN-major: advance 16 K-rows (two 8-row groups of 1024 bytes);
             // LBO = 8192 bytes between 64-wide atoms, SBO = 1024 between K groups.
+            // The same shared-memory offsets address the peer CTA's halves.
             const uint64_t adesc = A_MN ? smem_desc(sa + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
                                         : smem_desc(sa + kk * (UMMA_K * 2), 16, 1024);
             const uint64_t bdesc = B_MN ? smem_desc(sb + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
                                         : smem_desc(sb + kk * (UMMA_K * 2), 16, 1024);
             tc_mma(d, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          tc_commit(EMPTY(stage));
+          tc_commit_mc(EMPTY(stage), 0x3);  // both CTAs may refill this stage
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(ACCF(acc));
+        tc_commit_mc(ACCF(acc), 0x3);  // both CTAs' accumulators are ready
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       // all MMAs issued by this thread have completed once drain_bar flips
-      tc_commit(drain_bar);
+      tc_commit_mc(drain_bar, 0x1);
       volatile int no_abort = 0;
       wait_bounded(drain_bar, 0, Watch{&no_abort, p.err, p.timeout_ns});
     }
   } else if (EPI == EPI_AXPY) {
-    // ---------------------------------------------------------------- AXPY epilogue
+    // ---------------------------------------------------------------- AXPY epilogue (both CTAs)
     // X' = s (a (hi + lo) + acc) through shared memory: each warp stages a
     // 32 x 32 box of hi and of lo (TMA load, zero-filled past the edges),
     // overwrites it with hi' = bf16(X'), lo' = bf16(X' - hi') and TMA-stores
@@ -454,23 +497,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_load_3d(ebuf_s, &p.tm_src, ebar, col0_, row0_, m_);
       if (lo_in) tma_load_3d(ebuf_s + EPI_BOX_BYTES, &p.tm_src_lo, ebar, col0_, row0_, m_);
     };
+    const int rbase = (int)rank * BM + q * 32;  // this warp's rows within a pair tile
     int acc = 0;
     uint32_t acc_phase = 0;
-    long long t = blockIdx.x;
+    long long t = cid;
     int mat = 0, ti = 0, tj = 0;
     if (t < p.num_tiles) {
       decode_tile<EPI>(p, t, mat, ti, tj);
-      if (lane == 0) epi_load(mat, ti * BM + q * 32, tj * BN + half * 128);
+      if (lane == 0) epi_load(mat, ti * CM + rbase, tj * BN + half * 128);
     }
     bool alive = true;
-    for (; alive && t < p.num_tiles; t += gridDim.x) {
-      const long long tn = t + gridDim.x;
+    for (; alive && t < p.num_tiles; t += ncl) {
+      const long long tn = t + ncl;
       int mat_n = 0, ti_n = 0, tj_n = 0;
       if (tn < p.num_tiles) decode_tile<EPI>(p, tn, mat_n, ti_n, tj_n);
       const bool ok = wait_bounded(ACCF(acc), acc_phase, w);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int row0 = ti * BM + q * 32;
+      const int row0 = ti * CM + rbase;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS + half * 128);
       const float sc = p.scale ? p.scale[mat] : 1.0f;
 #pragma unroll 1
@@ -515,13 +559,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (ch + 1 < CHUNKS)
             epi_load(mat, row0, col0 + 32);
           else if (tn < p.num_tiles)
-            epi_load(mat_n, ti_n * BM + q * 32, tj_n * BN + half * 128);
+            epi_load(mat_n, ti_n * CM + rbase, tj_n * BN + half * 128);
         }
         __syncwarp();
       }
       if (!alive) break;
       tc_fence_before();
-      mbar_arrive(ACCE(acc));
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(ACCE(acc), 0));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
       mat = mat_n;
@@ -530,26 +575,27 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (lane == 0) bulk_wait_all();
   } else {
-    // ---------------------------------------------------------------- epilogue
+    // ---------------------------------------------------------------- SYRK / POLY epilogue (both CTAs)
     const int q = warp & 3;            // TMEM lane quadrant accessible to this warp
     const int half = (warp - 2) >> 2;  // which 128 columns of the tile
+    const int rbase = (int)rank * BM + q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    long long t = blockIdx.x;
+    long long t = cid;
     int mat = 0, ti = 0, tj = 0;
     Chunk cur, nxt;
     if (t < p.num_tiles) {
       decode_tile<EPI>(p, t, mat, ti, tj);
-      load_chunk<EPI>(p, mat, ti * BM + q * 32 + lane, tj * BN + half * 128, cur);
+      load_chunk<EPI>(p, mat, ti * CM + rbase, tj * BN + half * 128, cur);
     }
-    for (; t < p.num_tiles; t += gridDim.x) {
-      const long long tn = t + gridDim.x;
+    for (; t < p.num_tiles; t += ncl) {
+      const long long tn = t + ncl;
       int mat_n = 0, ti_n = 0, tj_n = 0;
       if (tn < p.num_tiles) decode_tile<EPI>(p, tn, mat_n, ti_n, tj_n);
       const bool ok = wait_bounded(ACCF(acc), acc_phase, w);
       if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: the TMEM loads below are .sync.aligned
       tc_fence_after();
-      const int row = ti * BM + q * 32 + lane;
+      const int row = ti * CM + rbase;
       const bool row_ok = row < p.M;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS + half * 128);
       const float sc = p.scale ? p.scale[mat] : 1.0f;
@@ -561,7 +607,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (ch + 1 < CHUNKS)
           load_chunk<EPI>(p, mat, row, col0 + 32, nxt);
         else if (tn < p.num_tiles)
-          load_chunk<EPI>(p, mat_n, ti_n * BM + q * 32 + lane, tj_n * BN + half * 128, nxt);
+          load_chunk<EPI>(p, mat_n, ti_n * CM + rbase, tj_n * BN + half * 128, nxt);
         uint32_t r[32];
         __syncwarp();
         tmem_ld32(taddr + (uint32_t)(ch * 32), r);
@@ -569,9 +615,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           float v[32];
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            Pack8 ch_hi, ch_lo;
-            ch_hi.v = cur.hi[g];
-            ch_lo.v = cur.lo[g];
+            Pack8 chh;
+            chh.v = cur.hi[g];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int k = g * 8 + 2 * e;
@@ -579,72 +624,41 @@ __global__ void __launch_bounds__(THREADS, 1)
               if (EPI == EPI_SYRK) {
                 v[k] = sc * a0;
                 v[k + 1] = sc * a1;
-              } else if (EPI == EPI_POLY) {
-                const float2 f = __bfloat1622float2(ch_hi.h[e]);
+              } else {
+                const float2 f = __bfloat1622float2(chh.h[e]);
                 v[k] = fmaf(p.c, a0, p.b * f.x);
                 v[k + 1] = fmaf(p.c, a1, p.b * f.y);
-              } else {
-                const float2 f = __bfloat1622float2(ch_hi.h[e]), fl = __bfloat1622float2(ch_lo.h[e]);
-                v[k] = sc * fmaf(p.a, f.x + fl.x, a0);
-                v[k + 1] = sc * fmaf(p.a, f.y + fl.y, a1);
               }
             }
           }
+          // symmetric output: (row, c) for c >= row, and the mirror (c, row) for c > row
           __nv_bfloat16 *orow = outm + (long long)row * p.out_ld;
-          if (EPI == EPI_AXPY) {
-            __nv_bfloat16 *lout =
-                p.out_lo ? p.out_lo + (long long)mat * p.out_mat + (long long)row * p.out_ld : nullptr;
-            if (col0 + 32 <= p.N) {
+          if (col0 >= row && col0 + 32 <= p.N) {
 #pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                Pack8 o, ol;
+            for (int g = 0; g < 4; ++g) {
+              Pack8 o;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int k = g * 8 + 2 * e;
-                  o.h[e] = __floats2bfloat162_rn(v[k], v[k + 1]);
-                  const float2 hh = __bfloat1622float2(o.h[e]);
-                  ol.h[e] = __floats2bfloat162_rn(v[k] - hh.x, v[k + 1] - hh.y);
-                }
-                reinterpret_cast<uint4 *>(orow + col0)[g] = o.v;
-                if (lout) reinterpret_cast<uint4 *>(lout + col0)[g] = ol.v;
-              }
-            } else {
-#pragma unroll
-              for (int k = 0; k < 32; ++k)
-                if (col0 + k < p.N) {
-                  const __nv_bfloat16 hh = __float2bfloat16_rn(v[k]);
-                  orow[col0 + k] = hh;
-                  if (lout) lout[col0 + k] = __float2bfloat16_rn(v[k] - __bfloat162float(hh));
-                }
+              for (int e = 0; e < 4; ++e) o.h[e] = __floats2bfloat162_rn(v[g * 8 + 2 * e], v[g * 8 + 2 * e + 1]);
+              reinterpret_cast<uint4 *>(orow + col0)[g] = o.v;
             }
           } else {
-            // symmetric output: (row, c) for c >= row, and the mirror (c, row) for c > row
-            if (col0 >= row && col0 + 32 <= p.N) {
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                Pack8 o;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o.h[e] = __floats2bfloat162_rn(v[g * 8 + 2 * e], v[g * 8 + 2 * e + 1]);
-                reinterpret_cast<uint4 *>(orow + col0)[g] = o.v;
-              }
-            } else {
-#pragma unroll
-              for (int k = 0; k < 32; ++k) {
-                const int c = col0 + k;
-                if (c >= row && c < p.N) orow[c] = __float2bfloat16_rn(v[k]);
-              }
-            }
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
               const int c = col0 + k;
-              if (c > row && c < p.N) outm[(long long)c * p.out_ld + row] = __float2bfloat16_rn(v[k]);
+              if (c >= row && c < p.N) orow[c] = __float2bfloat16_rn(v[k]);
             }
+          }
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int c = col0 + k;
+            if (c > row && c < p.N) outm[(long long)c * p.out_ld + row] = __float2bfloat16_rn(v[k]);
           }
         }
         cur = nxt;
       }
       tc_fence_before();
-      mbar_arrive(ACCE(acc));
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(ACCE(acc), 0));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
       mat = mat_n;
@@ -660,6 +674,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // no CTA frees TMEM or exits while its peer may still use them
   if (*abort_flag) {
     // let copies already in flight land before the shared memory is released
     const unsigned long long t0 = global_ns();
@@ -667,7 +682,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
   }
 }
 
@@ -721,18 +736,43 @@ template <int EPI, bool A_MN, bool B_MN>
 int launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int trace_kind, cudaStream_t s) {
   if (p.num_tiles == 0) return MUON_OK;
   static std::once_flag attr_once[64];
+  static int max_pairs[64];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MUON_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once[dev & 63], [&] {
+  std::call_once(attr_once[dev], [&] {
     attr_err =
         cudaFuncSetAttribute(ns_gemm_kernel<EPI, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    // a persistent grid must fit at once: launch no more pairs than can be co-resident
+    int n = 0;
+    cfg.gridDim = dim3(2 * (unsigned)std::max(1, num_sms() / 2), 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    if (attr_err == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&n, ns_gemm_kernel<EPI, A_MN, B_MN>, &cfg) == cudaSuccess && n > 0)
+      max_pairs[dev] = n;
+    else
+      max_pairs[dev] = std::max(1, num_sms() / 2);
+    cudaGetLastError();
   });
   if (attr_err != cudaSuccess) return MUON_ERR_CUDA;
-  const long long grid = std::min<long long>(p.num_tiles, num_sms());
+  // persistent CTA pairs over the tiles
+  const long long pairs = std::min<long long>(p.num_tiles, max_pairs[dev]);
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
   trace_before(trace_kind, s);
-  ns_gemm_kernel<EPI, A_MN, B_MN><<<(unsigned)grid, THREADS, SMEM_BYTES, s>>>(ma, mb, p);
-  return trace_after(trace_kind, s);
+  cudaError_t le = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<EPI, A_MN, B_MN>, ma, mb, p);
+  const int st = trace_after(trace_kind, s);
+  return le == cudaSuccess ? st : MUON_ERR_CUDA;
 }
 
 Params base_params(int M, int N, int K, int64_t batch) {
@@ -740,7 +780,7 @@ Params base_params(int M, int N, int K, int64_t batch) {
   p.M = M;
   p.N = N;
   p.K = K;
-  p.tiles_m = (M + BM - 1) / BM;
+  p.tiles_m = (M + CM - 1) / CM;
   p.tiles_n = (N + BN - 1) / BN;
   p.err = device_error_word();
   p.timeout_ns = wait_timeout_ns();
@@ -750,7 +790,7 @@ Params base_params(int M, int N, int K, int64_t batch) {
 
 int triangle_tiles(int tiles_m, int tiles_n) {
   int total = 0;
-  for (int i = 0; i < tiles_m; ++i) total += tiles_n - (i >> 1);
+  for (int i = 0; i < tiles_m; ++i) total += tiles_n - i;
   return total;
 }
 
@@ -760,9 +800,9 @@ int ns_syrk(const __nv_bfloat16 *X, __nv_bfloat16 *A, int64_t batch, int64_t m, 
             bool transposed, cudaStream_t s) {
   CUtensorMap ma, mb;
   int st;
-  if (!transposed) {  // X stored m x n: both operands K-major
+  if (!transposed) {  // X stored m x n: both operands K-major, 128-row boxes
     st = make_map(&ma, X, batch, m, n, BM);
-    if (!st) st = make_map(&mb, X, batch, m, n, BN);
+    mb = ma;
   } else {            // X stored n x m (X^T): both operands MN-major, 64 x 64 boxes
     st = make_map(&ma, X, batch, n, m, 64);
     mb = ma;
@@ -782,7 +822,7 @@ int ns_syrk(const __nv_bfloat16 *X, __nv_bfloat16 *A, int64_t batch, int64_t m, 
 int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, float b, float c, cudaStream_t s) {
   CUtensorMap ma, mb;
   int st = make_map(&ma, A, batch, m, m, BM);
-  if (!st) st = make_map(&mb, A, batch, m, m, BN);
+  mb = ma;
   if (st) return st;
   Params p = base_params((int)m, (int)m, (int)m, batch);
   p.tiles_per_mat = triangle_tiles(p.tiles_m, p.tiles_n);
@@ -813,7 +853,7 @@ int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 
   } else {
     // X stored n x m: X'^T = a X^T + X^T B (B symmetric), both operands K-major
     st = make_map(&ma, X, batch, n, m, BM);
-    if (!st) st = make_map(&mb, B, batch, m, m, BN);
+    if (!st) st = make_map(&mb, B, batch, m, m, BNH);
     p = base_params((int)n, (int)m, (int)m, batch);
     p.out_ld = m;
   }
