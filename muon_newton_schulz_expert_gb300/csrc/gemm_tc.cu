@@ -52,7 +52,17 @@ constexpr int BN = 256;    // columns of a pair tile
 constexpr int BNH = 128;   // rows of the B operand held by one CTA
 constexpr int BK = 64;     // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 6;
+// Shared-memory ring depth: the symmetric kernels use no epilogue staging and
+// take one more stage; AXPY gives that space to double-buffered staging.
+#ifndef MUON_STAGES_SYM
+#define MUON_STAGES_SYM 7
+#endif
+#ifndef MUON_STAGES_AXPY
+#define MUON_STAGES_AXPY 5
+#endif
+#ifndef MUON_EPI_SLOTS
+#define MUON_EPI_SLOTS 2
+#endif
 constexpr int A_STAGE = BM * BK * 2;   // 16 KB
 constexpr int B_STAGE = BNH * BK * 2;  // 16 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
@@ -60,16 +70,26 @@ constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 // half and one of its low half (64-byte swizzle), moved by TMA.
 constexpr int EPI_BOX = 32;
 constexpr int EPI_BOX_BYTES = EPI_BOX * EPI_BOX * 2;
-constexpr int EPI_BUF = 2 * EPI_BOX_BYTES;
+constexpr int EPI_BUF = 2 * EPI_BOX_BYTES;   // one slot: hi box + lo box
+constexpr int EPI_SLOTS = MUON_EPI_SLOTS;    // slots per epilogue warp
 constexpr int EPI_WARPS = 8;
-constexpr int NUM_BARS = 2 * STAGES + 5 + EPI_WARPS;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF + 1024 + NUM_BARS * 8 + 16;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer warp, MMA warp, 8 epilogue warps
 constexpr int ACC_COLS = BN;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int CHUNKS = BN / 2 / 32;  // 32-column chunks per epilogue thread and tile
+static_assert(CHUNKS % MUON_EPI_SLOTS == 0, "chunks per tile must fill the staging slots evenly");
 
 enum Epi { EPI_SYRK = 0, EPI_POLY = 1, EPI_AXPY = 2 };
+
+template <int EPI>
+struct Layout {
+  static constexpr int stages = EPI == EPI_AXPY ? MUON_STAGES_AXPY : MUON_STAGES_SYM;
+  static constexpr int epi_bytes = EPI == EPI_AXPY ? EPI_WARPS * EPI_SLOTS * EPI_BUF : 0;
+  static constexpr int num_bars = 2 * stages + 5 + EPI_WARPS * EPI_SLOTS;
+  static constexpr int smem_bytes = stages * STAGE_BYTES + epi_bytes + 1024 + num_bars * 8 + 16;
+};
+static_assert(Layout<EPI_AXPY>::smem_bytes <= 232448, "AXPY shared memory");
+static_assert(Layout<EPI_SYRK>::smem_bytes <= 232448, "SYRK/POLY shared memory");
 
 struct Params {
   // AXPY epilogue maps (32 x 32 boxes): X high half, X low half, X' high, X' low
@@ -329,9 +349,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *epi_smem = smem + STAGES * STAGE_BYTES;  // EPI_WARPS staging buffers, 1024-aligned
-  uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + EPI_WARPS * EPI_BUF);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
+  constexpr int STAGES = Layout<EPI>::stages;
+  uint8_t *epi_smem = smem + STAGES * STAGE_BYTES;  // AXPY staging slots, 1024-aligned
+  uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + Layout<EPI>::epi_bytes);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Layout<EPI>::num_bars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const uint32_t sbase = smem_u32(smem);
@@ -356,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(ACCE(a), 2 * EPI_WARPS);     // used in CTA 0: every epilogue warp of the pair
     }
     mbar_init(drain_bar, 1);
-    for (int e = 0; e < EPI_WARPS; ++e) mbar_init(EBAR(e), 1);
+    for (int e = 0; e < EPI_WARPS * EPI_SLOTS; ++e) mbar_init(EBAR(e), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -483,19 +504,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     // overwrites it with hi' = bf16(X'), lo' = bf16(X' - hi') and TMA-stores
     // it (clipped at the edges).  Lane i owns row i of the box, which is TMEM
     // lane 32q + i; the 64-byte swizzle makes these row reads conflict-free.
+    // With two slots per warp the box of chunk g + 2 is fetched into the slot
+    // of chunk g as soon as g's store has read it, a whole chunk ahead of use.
     const int ew = warp - 2;
     const int q = warp & 3, half = ew >> 2;
-    uint8_t *ebuf = epi_smem + ew * EPI_BUF;   // [hi box][lo box]
-    const uint32_t ebuf_s = smem_u32(ebuf);
-    const uint32_t ebar = EBAR(ew);
-    uint32_t ephase = 0;
+    uint8_t *ebase = epi_smem + ew * EPI_SLOTS * EPI_BUF;   // slots of [hi box][lo box]
+    const uint32_t ebase_s = smem_u32(ebase);
+    uint32_t ephase_bits = 0;                                // parity per slot
     const bool lo_in = p.src_lo != nullptr, lo_out = p.out_lo != nullptr;
     const uint32_t etx = lo_in ? 2u * EPI_BOX_BYTES : (uint32_t)EPI_BOX_BYTES;
-    auto epi_load = [&](int m_, int row0_, int col0_) {  // lane 0 only
+    auto epi_load = [&](int slot, int m_, int row0_, int col0_) {  // lane 0 only
+      const uint32_t dst = ebase_s + slot * EPI_BUF, bar = EBAR(ew * EPI_SLOTS + slot);
       fence_proxy_async_smem();
-      mbar_expect_tx(ebar, etx);
-      tma_load_3d(ebuf_s, &p.tm_src, ebar, col0_, row0_, m_);
-      if (lo_in) tma_load_3d(ebuf_s + EPI_BOX_BYTES, &p.tm_src_lo, ebar, col0_, row0_, m_);
+      mbar_expect_tx(bar, etx);
+      tma_load_3d(dst, &p.tm_src, bar, col0_, row0_, m_);
+      if (lo_in) tma_load_3d(dst + EPI_BOX_BYTES, &p.tm_src_lo, bar, col0_, row0_, m_);
     };
     const int rbase = (int)rank * BM + q * 32;  // this warp's rows within a pair tile
     int acc = 0;
@@ -504,7 +527,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     int mat = 0, ti = 0, tj = 0;
     if (t < p.num_tiles) {
       decode_tile<EPI>(p, t, mat, ti, tj);
-      if (lane == 0) epi_load(mat, ti * CM + rbase, tj * BN + half * 128);
+      if (lane == 0)
+        for (int c = 0; c < EPI_SLOTS; ++c) epi_load(c, mat, ti * CM + rbase, tj * BN + half * 128 + c * 32);
     }
     bool alive = true;
     for (; alive && t < p.num_tiles; t += ncl) {
@@ -519,13 +543,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float sc = p.scale ? p.scale[mat] : 1.0f;
 #pragma unroll 1
       for (int ch = 0; ch < CHUNKS; ++ch) {
+        const int slot = ch % EPI_SLOTS;   // CHUNKS is a multiple of EPI_SLOTS
+        uint8_t *ebuf = ebase + slot * EPI_BUF;
         const int col0 = tj * BN + half * 128 + ch * 32;
-        const bool got = wait_bounded(ebar, ephase, w);
+        const bool got = wait_bounded(EBAR(ew * EPI_SLOTS + slot), (ephase_bits >> slot) & 1u, w);
         if (!__all_sync(0xffffffffu, got)) {
           alive = false;
           break;
         }
-        ephase ^= 1u;
+        ephase_bits ^= 1u << slot;
         uint32_t r[32];
         __syncwarp();
         tmem_ld32(taddr + (uint32_t)(ch * 32), r);
@@ -551,15 +577,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_3d(&p.tm_out, ebuf_s, col0, row0, mat);
-          if (lo_out) tma_store_3d(&p.tm_out_lo, ebuf_s + EPI_BOX_BYTES, col0, row0, mat);
+          const uint32_t src = ebase_s + slot * EPI_BUF;
+          tma_store_3d(&p.tm_out, src, col0, row0, mat);
+          if (lo_out) tma_store_3d(&p.tm_out_lo, src + EPI_BOX_BYTES, col0, row0, mat);
           bulk_commit();
           bulk_wait_read_all();
-          // the staging box is free again: fetch the next chunk's operands
-          if (ch + 1 < CHUNKS)
-            epi_load(mat, row0, col0 + 32);
+          // this slot is free again: fetch chunk ch + EPI_SLOTS (possibly of the next tile)
+          const int nc = ch + EPI_SLOTS;
+          if (nc < CHUNKS)
+            epi_load(slot, mat, row0, col0 + EPI_SLOTS * 32);
           else if (tn < p.num_tiles)
-            epi_load(mat_n, ti_n * CM + rbase, tj_n * BN + half * 128);
+            epi_load(slot, mat_n, ti_n * CM + rbase, tj_n * BN + half * 128 + (nc - CHUNKS) * 32);
         }
         __syncwarp();
       }
@@ -751,11 +779,12 @@ int launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int tr
   cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once[dev], [&] {
     attr_err =
-        cudaFuncSetAttribute(ns_gemm_kernel<EPI, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaFuncSetAttribute(ns_gemm_kernel<EPI, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Layout<EPI>::smem_bytes);
     // a persistent grid must fit at once: launch no more pairs than can be co-resident
     int n = 0;
     cfg.gridDim = dim3(2 * (unsigned)std::max(1, num_sms() / 2), 1, 1);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = Layout<EPI>::smem_bytes;
     if (attr_err == cudaSuccess &&
         cudaOccupancyMaxActiveClusters(&n, ns_gemm_kernel<EPI, A_MN, B_MN>, &cfg) == cudaSuccess && n > 0)
       max_pairs[dev] = n;
@@ -767,7 +796,7 @@ int launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int tr
   // persistent CTA pairs over the tiles
   const long long pairs = std::min<long long>(p.num_tiles, max_pairs[dev]);
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = Layout<EPI>::smem_bytes;
   cfg.stream = s;
   trace_before(trace_kind, s);
   cudaError_t le = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<EPI, A_MN, B_MN>, ma, mb, p);
