@@ -52,16 +52,27 @@ constexpr int BN = 256;    // columns of a pair tile
 constexpr int BNH = 128;   // rows of the B operand held by one CTA
 constexpr int BK = 64;     // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
-// Shared-memory ring depth: the symmetric kernels use no epilogue staging and
-// take one more stage; AXPY gives that space to double-buffered staging.
-#ifndef MUON_STAGES_SYM
-#define MUON_STAGES_SYM 7
+// Shared-memory split between the operand ring and the epilogue staging
+// slots (one slot = two 2 KB boxes per epilogue warp).  X X^T has a long K
+// loop and no epilogue operand: deeper ring, one slot.  The short-K kernels
+// stream an epilogue operand: two slots, so each box is fetched a chunk ahead.
+#ifndef MUON_STAGES_SYRK
+#define MUON_STAGES_SYRK 6
+#endif
+#ifndef MUON_SLOTS_SYRK
+#define MUON_SLOTS_SYRK 1
+#endif
+#ifndef MUON_STAGES_POLY
+#define MUON_STAGES_POLY 5
+#endif
+#ifndef MUON_SLOTS_POLY
+#define MUON_SLOTS_POLY 2
 #endif
 #ifndef MUON_STAGES_AXPY
 #define MUON_STAGES_AXPY 5
 #endif
-#ifndef MUON_EPI_SLOTS
-#define MUON_EPI_SLOTS 2
+#ifndef MUON_SLOTS_AXPY
+#define MUON_SLOTS_AXPY 2
 #endif
 constexpr int A_STAGE = BM * BK * 2;   // 16 KB
 constexpr int B_STAGE = BNH * BK * 2;  // 16 KB
@@ -70,30 +81,32 @@ constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 // half and one of its low half (64-byte swizzle), moved by TMA.
 constexpr int EPI_BOX = 32;
 constexpr int EPI_BOX_BYTES = EPI_BOX * EPI_BOX * 2;
-constexpr int EPI_BUF = 2 * EPI_BOX_BYTES;   // one slot: hi box + lo box
-constexpr int EPI_SLOTS = MUON_EPI_SLOTS;    // slots per epilogue warp
+constexpr int EPI_BUF = 2 * EPI_BOX_BYTES;   // one slot: two boxes
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer warp, MMA warp, 8 epilogue warps
 constexpr int ACC_COLS = BN;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int CHUNKS = BN / 2 / 32;  // 32-column chunks per epilogue thread and tile
-static_assert(CHUNKS % MUON_EPI_SLOTS == 0, "chunks per tile must fill the staging slots evenly");
 
 enum Epi { EPI_SYRK = 0, EPI_POLY = 1, EPI_AXPY = 2 };
 
 template <int EPI>
 struct Layout {
-  static constexpr int stages = EPI == EPI_AXPY ? MUON_STAGES_AXPY : MUON_STAGES_SYM;
-  static constexpr int epi_bytes = EPI == EPI_AXPY ? EPI_WARPS * EPI_SLOTS * EPI_BUF : 0;
-  static constexpr int num_bars = 2 * stages + 5 + EPI_WARPS * EPI_SLOTS;
+  static constexpr int stages =
+      EPI == EPI_AXPY ? MUON_STAGES_AXPY : (EPI == EPI_POLY ? MUON_STAGES_POLY : MUON_STAGES_SYRK);
+  static constexpr int slots = EPI == EPI_AXPY ? MUON_SLOTS_AXPY : (EPI == EPI_POLY ? MUON_SLOTS_POLY : MUON_SLOTS_SYRK);
+  static constexpr int epi_bytes = EPI_WARPS * slots * EPI_BUF;
+  static constexpr int num_bars = 2 * stages + 5 + EPI_WARPS * slots;
   static constexpr int smem_bytes = stages * STAGE_BYTES + epi_bytes + 1024 + num_bars * 8 + 16;
+  static_assert(CHUNKS % slots == 0, "chunks per tile must fill the staging slots evenly");
+  static_assert(smem_bytes <= 232448, "shared memory per CTA");
 };
-static_assert(Layout<EPI_AXPY>::smem_bytes <= 232448, "AXPY shared memory");
-static_assert(Layout<EPI_SYRK>::smem_bytes <= 232448, "SYRK/POLY shared memory");
 
 struct Params {
-  // AXPY epilogue maps (32 x 32 boxes): X high half, X low half, X' high, X' low
-  CUtensorMap tm_src, tm_src_lo, tm_out, tm_out_lo;
+  // epilogue maps, 32 x 32 boxes.  AXPY: X high half, X low half, X' high,
+  // X' low.  SYRK/POLY: A (POLY's operand), the output, and the output again
+  // without swizzle for the transposed (mirror) boxes.
+  CUtensorMap tm_src, tm_src_lo, tm_out, tm_out_lo, tm_out_t;
   int M, N, K;                 // output M x N, reduction length K (per matrix)
   int tiles_m, tiles_n;        // pair tiles of 256 x 256
   int tiles_per_mat;
@@ -313,36 +326,6 @@ union Pack8 {
   __nv_bfloat162 h[4];
 };
 
-// Epilogue operands of one thread for one 32-column chunk of its row
-// (POLY: A in hi).  AXPY stages its operands through shared memory instead.
-struct Chunk {
-  uint4 hi[4];
-};
-
-template <int EPI>
-__device__ __forceinline__ void load_chunk(const Params &p, int mat, int row, int col0, Chunk &c) {
-  if (EPI != EPI_POLY) return;
-  const bool valid = row < p.M && col0 < p.N;
-  const __nv_bfloat16 *srow = p.src + (long long)mat * p.src_mat + (long long)row * p.src_ld + col0;
-  if (valid && col0 + 32 <= p.N) {
-#pragma unroll
-    for (int g = 0; g < 4; ++g) c.hi[g] = __ldg(reinterpret_cast<const uint4 *>(srow) + g);
-  } else {
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      Pack8 th;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int k0 = g * 8 + 2 * e;
-        const bool ok0 = valid && col0 + k0 < p.N, ok1 = valid && col0 + k0 + 1 < p.N;
-        th.h[e] = __floats2bfloat162_rn(ok0 ? __bfloat162float(srow[k0]) : 0.f,
-                                        ok1 ? __bfloat162float(srow[k0 + 1]) : 0.f);
-      }
-      c.hi[g] = th.v;
-    }
-  }
-}
-
 template <int EPI, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(THREADS, 1)
     ns_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -377,7 +360,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(ACCE(a), 2 * EPI_WARPS);     // used in CTA 0: every epilogue warp of the pair
     }
     mbar_init(drain_bar, 1);
-    for (int e = 0; e < EPI_WARPS * EPI_SLOTS; ++e) mbar_init(EBAR(e), 1);
+    for (int e = 0; e < EPI_WARPS * Layout<EPI>::slots; ++e) mbar_init(EBAR(e), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -506,15 +489,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     // lane 32q + i; the 64-byte swizzle makes these row reads conflict-free.
     // With two slots per warp the box of chunk g + 2 is fetched into the slot
     // of chunk g as soon as g's store has read it, a whole chunk ahead of use.
+    constexpr int SLOTS = Layout<EPI>::slots;
     const int ew = warp - 2;
     const int q = warp & 3, half = ew >> 2;
-    uint8_t *ebase = epi_smem + ew * EPI_SLOTS * EPI_BUF;   // slots of [hi box][lo box]
+    uint8_t *ebase = epi_smem + ew * SLOTS * EPI_BUF;   // slots of [hi box][lo box]
     const uint32_t ebase_s = smem_u32(ebase);
     uint32_t ephase_bits = 0;                                // parity per slot
     const bool lo_in = p.src_lo != nullptr, lo_out = p.out_lo != nullptr;
     const uint32_t etx = lo_in ? 2u * EPI_BOX_BYTES : (uint32_t)EPI_BOX_BYTES;
     auto epi_load = [&](int slot, int m_, int row0_, int col0_) {  // lane 0 only
-      const uint32_t dst = ebase_s + slot * EPI_BUF, bar = EBAR(ew * EPI_SLOTS + slot);
+      const uint32_t dst = ebase_s + slot * EPI_BUF, bar = EBAR(ew * SLOTS + slot);
       fence_proxy_async_smem();
       mbar_expect_tx(bar, etx);
       tma_load_3d(dst, &p.tm_src, bar, col0_, row0_, m_);
@@ -528,7 +512,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (t < p.num_tiles) {
       decode_tile<EPI>(p, t, mat, ti, tj);
       if (lane == 0)
-        for (int c = 0; c < EPI_SLOTS; ++c) epi_load(c, mat, ti * CM + rbase, tj * BN + half * 128 + c * 32);
+        for (int c = 0; c < SLOTS; ++c) epi_load(c, mat, ti * CM + rbase, tj * BN + half * 128 + c * 32);
     }
     bool alive = true;
     for (; alive && t < p.num_tiles; t += ncl) {
@@ -543,10 +527,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float sc = p.scale ? p.scale[mat] : 1.0f;
 #pragma unroll 1
       for (int ch = 0; ch < CHUNKS; ++ch) {
-        const int slot = ch % EPI_SLOTS;   // CHUNKS is a multiple of EPI_SLOTS
+        const int slot = ch % SLOTS;   // CHUNKS is a multiple of SLOTS
         uint8_t *ebuf = ebase + slot * EPI_BUF;
         const int col0 = tj * BN + half * 128 + ch * 32;
-        const bool got = wait_bounded(EBAR(ew * EPI_SLOTS + slot), (ephase_bits >> slot) & 1u, w);
+        const bool got = wait_bounded(EBAR(ew * SLOTS + slot), (ephase_bits >> slot) & 1u, w);
         if (!__all_sync(0xffffffffu, got)) {
           alive = false;
           break;
@@ -582,10 +566,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (lo_out) tma_store_3d(&p.tm_out_lo, src + EPI_BOX_BYTES, col0, row0, mat);
           bulk_commit();
           bulk_wait_read_all();
-          // this slot is free again: fetch chunk ch + EPI_SLOTS (possibly of the next tile)
-          const int nc = ch + EPI_SLOTS;
+          // this slot is free again: fetch chunk ch + SLOTS (possibly of the next tile)
+          const int nc = ch + SLOTS;
           if (nc < CHUNKS)
-            epi_load(slot, mat, row0, col0 + EPI_SLOTS * 32);
+            epi_load(slot, mat, row0, col0 + SLOTS * 32);
           else if (tn < p.num_tiles)
             epi_load(slot, mat_n, ti_n * CM + rbase, tj_n * BN + half * 128 + (nc - CHUNKS) * 32);
         }
@@ -604,86 +588,142 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) bulk_wait_all();
   } else {
     // ---------------------------------------------------------------- SYRK / POLY epilogue (both CTAs)
-    const int q = warp & 3;            // TMEM lane quadrant accessible to this warp
-    const int half = (warp - 2) >> 2;  // which 128 columns of the tile
-    const int rbase = (int)rank * BM + q * 32 + lane;
+    // Each warp's 32 x 32 chunk (rows row0.., columns col0.., both multiples
+    // of 32) lies strictly above the diagonal, strictly below it, or on it.
+    // Above: the values go through shared memory to two TMA stores, the box
+    // itself (64-byte swizzle) and its transpose (the mirror, written as
+    // [column][row] without swizzle).  Below: nothing (the mirror of another
+    // chunk covers it).  On the diagonal: element stores, (r, c >= r) and the
+    // mirror (c, r) for c > r.  POLY's operand b*A arrives by TMA in the box.
+    constexpr int SLOTS = Layout<EPI>::slots;
+    const int ew = warp - 2;
+    const int q = warp & 3, half = ew >> 2;
+    uint8_t *ebase = epi_smem + ew * SLOTS * EPI_BUF;   // slots of [direct box][mirror box]
+    const uint32_t ebase_s = smem_u32(ebase);
+    uint32_t ephase_bits = 0;
+    const int rbase = (int)rank * BM + q * 32;
+    auto needs_load = [&](int row0_, int col0_) {
+      return EPI == EPI_POLY && col0_ + 32 > row0_ && row0_ < p.M && col0_ < p.N;
+    };
+    auto epi_load = [&](int slot, int m_, int row0_, int col0_) {  // lane 0 only
+      const uint32_t bar = EBAR(ew * SLOTS + slot);
+      fence_proxy_async_smem();
+      mbar_expect_tx(bar, EPI_BOX_BYTES);
+      tma_load_3d(ebase_s + slot * EPI_BUF, &p.tm_src, bar, col0_, row0_, m_);
+    };
     int acc = 0;
     uint32_t acc_phase = 0;
     long long t = cid;
     int mat = 0, ti = 0, tj = 0;
-    Chunk cur, nxt;
     if (t < p.num_tiles) {
       decode_tile<EPI>(p, t, mat, ti, tj);
-      load_chunk<EPI>(p, mat, ti * CM + rbase, tj * BN + half * 128, cur);
+      if (lane == 0)
+        for (int c = 0; c < SLOTS; ++c) {
+          const int r0 = ti * CM + rbase, c0 = tj * BN + half * 128 + c * 32;
+          if (needs_load(r0, c0)) epi_load(c, mat, r0, c0);
+        }
     }
-    for (; t < p.num_tiles; t += ncl) {
+    bool alive = true;
+    for (; alive && t < p.num_tiles; t += ncl) {
       const long long tn = t + ncl;
       int mat_n = 0, ti_n = 0, tj_n = 0;
       if (tn < p.num_tiles) decode_tile<EPI>(p, tn, mat_n, ti_n, tj_n);
       const bool ok = wait_bounded(ACCF(acc), acc_phase, w);
       if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform: the TMEM loads below are .sync.aligned
       tc_fence_after();
-      const int row = ti * CM + rbase;
-      const bool row_ok = row < p.M;
+      const int row0 = ti * CM + rbase;
+      const int row = row0 + lane;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS + half * 128);
       const float sc = p.scale ? p.scale[mat] : 1.0f;
       __nv_bfloat16 *outm = p.out + (long long)mat * p.out_mat;
 #pragma unroll 1
       for (int ch = 0; ch < CHUNKS; ++ch) {
+        const int slot = ch % SLOTS;
+        uint8_t *ebuf = ebase + slot * EPI_BUF;
         const int col0 = tj * BN + half * 128 + ch * 32;
-        // prefetch the operands of the next chunk (or of the next tile's first chunk)
-        if (ch + 1 < CHUNKS)
-          load_chunk<EPI>(p, mat, row, col0 + 32, nxt);
-        else if (tn < p.num_tiles)
-          load_chunk<EPI>(p, mat_n, ti_n * CM + rbase, tj_n * BN + half * 128, nxt);
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(taddr + (uint32_t)(ch * 32), r);
-        if (row_ok && col0 < p.N) {
+        const bool in_range = row0 < p.M && col0 < p.N;
+        const bool above = col0 >= row0 + 32, below = col0 + 32 <= row0;
+        if (needs_load(row0, col0)) {
+          const bool got = wait_bounded(EBAR(ew * SLOTS + slot), (ephase_bits >> slot) & 1u, w);
+          if (!__all_sync(0xffffffffu, got)) {
+            alive = false;
+            break;
+          }
+          ephase_bits ^= 1u << slot;
+        }
+        if (in_range && !below) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld32(taddr + (uint32_t)(ch * 32), r);
           float v[32];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            Pack8 chh;
-            chh.v = cur.hi[g];
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t off = (uint32_t)(lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
+            Pack8 av;
+            if (EPI == EPI_POLY) av.v = *reinterpret_cast<const uint4 *>(ebuf + off);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int k = g * 8 + 2 * e;
+              const int k = c * 8 + 2 * e;
               const float a0 = __uint_as_float(r[k]), a1 = __uint_as_float(r[k + 1]);
               if (EPI == EPI_SYRK) {
                 v[k] = sc * a0;
                 v[k + 1] = sc * a1;
               } else {
-                const float2 f = __bfloat1622float2(chh.h[e]);
+                const float2 f = __bfloat1622float2(av.h[e]);
                 v[k] = fmaf(p.c, a0, p.b * f.x);
                 v[k + 1] = fmaf(p.c, a1, p.b * f.y);
               }
             }
           }
-          // symmetric output: (row, c) for c >= row, and the mirror (c, row) for c > row
-          __nv_bfloat16 *orow = outm + (long long)row * p.out_ld;
-          if (col0 >= row && col0 + 32 <= p.N) {
+          if (above) {
+            // direct box [row][col] (swizzled) and mirror box [col][row]
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t off = (uint32_t)(lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
               Pack8 o;
 #pragma unroll
-              for (int e = 0; e < 4; ++e) o.h[e] = __floats2bfloat162_rn(v[g * 8 + 2 * e], v[g * 8 + 2 * e + 1]);
-              reinterpret_cast<uint4 *>(orow + col0)[g] = o.v;
+              for (int e = 0; e < 4; ++e) o.h[e] = __floats2bfloat162_rn(v[c * 8 + 2 * e], v[c * 8 + 2 * e + 1]);
+              *reinterpret_cast<uint4 *>(ebuf + off) = o.v;
+            }
+            __nv_bfloat16 *mb = reinterpret_cast<__nv_bfloat16 *>(ebuf + EPI_BOX_BYTES);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) mb[k * 32 + lane] = __float2bfloat16_rn(v[k]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const uint32_t src = ebase_s + slot * EPI_BUF;
+              tma_store_3d(&p.tm_out, src, col0, row0, mat);
+              tma_store_3d(&p.tm_out_t, src + EPI_BOX_BYTES, row0, col0, mat);
+              bulk_commit();
             }
           } else {
+            // on the diagonal
+            __nv_bfloat16 *orow = outm + (long long)row * p.out_ld;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
               const int c = col0 + k;
-              if (c >= row && c < p.N) orow[c] = __float2bfloat16_rn(v[k]);
+              if (row < p.M && c < p.N) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(v[k]);
+                if (c >= row) orow[c] = h;
+                if (c > row) outm[(long long)c * p.out_ld + row] = h;
+              }
             }
           }
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int c = col0 + k;
-            if (c > row && c < p.N) outm[(long long)c * p.out_ld + row] = __float2bfloat16_rn(v[k]);
+        }
+        if (lane == 0) {
+          // the slot's stores have read it: refill it with chunk ch + SLOTS
+          bulk_wait_read_all();
+          const int nc = ch + SLOTS;
+          if (nc < CHUNKS) {
+            if (needs_load(row0, col0 + SLOTS * 32)) epi_load(slot, mat, row0, col0 + SLOTS * 32);
+          } else if (tn < p.num_tiles) {
+            const int r0 = ti_n * CM + rbase, c0 = tj_n * BN + half * 128 + (nc - CHUNKS) * 32;
+            if (needs_load(r0, c0)) epi_load(slot, mat_n, r0, c0);
           }
         }
-        cur = nxt;
+        __syncwarp();
       }
+      if (!alive) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_rank(ACCE(acc), 0));
@@ -693,6 +733,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       ti = ti_n;
       tj = tj_n;
     }
+    if (lane == 0) bulk_wait_all();
   }
 #undef FULL
 #undef EMPTY
@@ -838,6 +879,9 @@ int ns_syrk(const __nv_bfloat16 *X, __nv_bfloat16 *A, int64_t batch, int64_t m, 
   }
   if (st) return st;
   Params p = base_params((int)m, (int)m, (int)n, batch);
+  st = make_map(&p.tm_out, A, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!st) st = make_map(&p.tm_out_t, A, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st) return st;
   p.tiles_per_mat = triangle_tiles(p.tiles_m, p.tiles_n);
   p.num_tiles = (long long)p.tiles_per_mat * batch;
   p.out = A;
@@ -854,6 +898,10 @@ int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, 
   mb = ma;
   if (st) return st;
   Params p = base_params((int)m, (int)m, (int)m, batch);
+  st = make_map(&p.tm_src, A, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!st) st = make_map(&p.tm_out, B, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!st) st = make_map(&p.tm_out_t, B, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st) return st;
   p.tiles_per_mat = triangle_tiles(p.tiles_m, p.tiles_n);
   p.num_tiles = (long long)p.tiles_per_mat * batch;
   p.out = B;
