@@ -85,6 +85,27 @@ def aggregate_value(matrices_per_rank, world, ms_per_step_max):
     return matrices_per_rank * world / (ms_per_step_max / 1e3)
 
 
+def axpy_traffic_per_matrix():
+    """DRAM bytes per matrix of ns_axpy_tc from the committed ncu summary, or None
+    when the kernel source changed after the counters were taken."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "ns_gemm_kernels_profile8.md")
+    src = os.path.join(ROOT, "muon_newton_schulz_expert_gb300", "csrc", "gemm_tc.cu")
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    fields = {}
+    with open(prof) as f:
+        for line in f:
+            if ":" in line and line.split(":")[0] in ("traffic_bytes_per_matrix", "source_sha256"):
+                k, v = line.split(":", 1)
+                fields[k] = v.strip()
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    if fields.get("source_sha256") != sha or "traffic_bytes_per_matrix" not in fields:
+        return None
+    return int(fields["traffic_bytes_per_matrix"])
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -284,6 +305,7 @@ def run_gpu(args):
                "copies": "pinned host, side streams overlapped with compute"}
 
     peaks, peak_src = load_peaks()
+    adamw = None if args.no_adamw else bench_adamw(mk, torch, dev, stream, float(peaks.get("hbm_gbs", 6800.0)))
     kernels = {}
     for name, (n, t) in sorted(trace.items()):
         ent = {"launches": n, "avg_ms": round(t / n, 4), "share": None}
@@ -305,8 +327,12 @@ def run_gpu(args):
     dn, dt = trace[dom]
     achieved = KERNEL_FLOPS[dom] * 5 * total * args.steps / (dt / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    traffic = args.traffic
+    if traffic is None and dom == "ns_axpy_tc" and axpy_traffic_per_matrix():
+        traffic = axpy_traffic_per_matrix() * total / len(groups)   # bytes per average launch
     roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-            "frac": round(achieved / peak, 4), "traffic": args.traffic,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "traffic_note": "ncu dram read+write bytes per matrix (8-matrix capture) x matrices per launch",
             "peak_source": f"bf16_tflops_sustained ({peak_src})",
             "avg_launch_ms": round(dt / dn, 4), "launches": dn}
     tc_ms = sum(trace.get(k, (0, 0.0))[1] for k in KERNEL_FLOPS) / args.steps
@@ -325,6 +351,7 @@ def run_gpu(args):
         "tensor_kernels_tflops": round(total * FLOPS_NS / (tc_ms / 1e3) / 1e12, 1) if tc_ms else None,
         "flops_per_matrix": {"algorithmic_symmetric": FLOPS_NS, "dense_equivalent": FLOPS_NS_DENSE},
         "roofline": roof, "kernels": kernels, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
+        "adamw": adamw,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -332,6 +359,34 @@ def run_gpu(args):
         print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def bench_adamw(mk, torch, dev, stream, hbm_peak, steps=10, warmup=3):
+    """AdamW on an embedding-shaped table (vocabulary 256000 x hidden 6144 of the
+    model-configuration table): bf16 parameters and gradients, fp32 moments.
+    22 algorithmic HBM bytes per element (read W, g, m, v; write W, m, v)."""
+    numel = 256000 * 6144
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(97)
+    W = (torch.randn(numel, generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+    g = (torch.randn(numel, generator=gen, device=dev) * 1e-2).to(torch.bfloat16)
+    m = torch.zeros(numel, device=dev)
+    v = torch.zeros(numel, device=dev)
+    for t in range(1, warmup + 1):
+        mk.muon_adamw_update(W, g, m, v, t, stream=stream)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for t in range(warmup + 1, warmup + steps + 1):
+        mk.muon_adamw_update(W, g, m, v, t, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    gbs = 22 * numel / (ms / 1e3) / 1e9
+    del W, g, m, v
+    return {"workload": "embedding table 256000x6144, bf16 params/grads, fp32 moments (inputs > L2)",
+            "ms_per_update": round(ms, 4), "achieved": round(gbs, 1), "unit": "GB/s", "bound": "hbm",
+            "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4), "bytes_per_element": 22}
 
 
 # ----------------------------------------------------------------------------- the oracle on the host cores
@@ -415,6 +470,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-adamw", action="store_true", help="skip the AdamW (routers/embeddings) measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="rank96", choices=["rank96", "profile8"],
                     help="rank96: the 96-matrix bench workload; profile8: 8 matrices for ncu captures")

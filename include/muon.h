@@ -81,7 +81,7 @@ int muon_momentum_update_f32(const float *grad, float *momentum, float *update_o
  *           the result in the same layout.  m > n is accepted: the iteration
  *           runs on X^T and the result is written back in X's layout.
  *   batch   >= 0 (0 is a no-op), m >= 1, n >= 1
- *   steps   >= 0 (0 = normalisation only)
+ *   steps   0..1000 (0 = normalisation only)
  *   coeffs  host pointer to 3 floats (a, b, c); the quintic is
  *           (3.4445, -4.7750, 2.0315)
  *   eps     added to the Frobenius norm, eps >= 0 (1e-7 by convention)
@@ -104,6 +104,18 @@ int muon_ns_batched(void *X, int64_t batch, int64_t m, int64_t n, int steps, con
 size_t muon_ns_workspace_bytes(int64_t batch, int64_t m, int64_t n);
 int muon_ns_batched_ws(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3],
                        float eps, void *workspace, size_t workspace_bytes, muon_stream_t stream);
+
+/* Coefficient schedules (FlexShard section: "a few" Newton-Schulz iterations;
+ * the page fixes neither their number nor their constants).  Step it uses
+ * (a, b, c) = coeffs[3*it .. 3*it+2]; `coeffs` is a host array of 3*steps
+ * floats (any non-null pointer when steps == 0).  Everything else as
+ * muon_ns_batched / muon_ns_batched_f32, including the stream-ordered
+ * workspace.  A schedule whose rows are all equal gives exactly the result of
+ * the constant-coefficient call. */
+int muon_ns_batched_schedule(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float *coeffs,
+                             float eps, muon_stream_t stream);
+int muon_ns_batched_schedule_f32(float *X, int64_t batch, int64_t m, int64_t n, int steps, const float *coeffs,
+                                 float eps, muon_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Newton-Schulz that allocates nothing.  The paper has no counterpart: this
@@ -155,6 +167,29 @@ int muon_apply_update(void *param, const void *update, int64_t batch, int64_t ro
 /* fp32 parameter and update, same formula without the bf16 rounding. */
 int muon_apply_update_f32(float *param, const float *update, int64_t batch, int64_t rows, int64_t cols,
                           float lr, float weight_decay, float scale, muon_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * AdamW for the parameters Muon does not take (FlexShard section: routers and
+ * embeddings use AdamW, with two fp32 states per parameter).  Reading taken:
+ * decoupled weight decay with bias correction, every fp32 operation rounded
+ * separately in this order (bit-reproducible):
+ *   m <- (b1*m) + (c1*g);  v <- (b2*v) + (c2*(g*g));
+ *   d <- sqrt(v / bc2) + eps;  W <- (kw*W) - (step_size*(m / d))
+ * with c1 = 1-beta1, c2 = 1-beta2, bc2 = 1-beta2^step, step_size =
+ * lr/(1-beta1^step), kw = 1-lr*weight_decay formed in double from the float
+ * arguments and rounded once to fp32.
+ *   param       device, bf16 (or fp32 for _f32), numel elements, in place
+ *   grad        device, bf16 (fp32), numel elements
+ *   exp_avg     device, fp32 first moment, in place;  exp_avg_sq: second moment
+ *   step        >= 1, the 1-based step count the bias correction uses
+ * Errors: MUON_ERR_INVALID_ARG for null pointers (numel > 0), numel < 0,
+ * step < 1, betas outside [0, 1), negative eps or non-finite arguments.
+ */
+int muon_adamw_update(void *param, const void *grad, float *exp_avg, float *exp_avg_sq, int64_t numel, float lr,
+                      float beta1, float beta2, float eps, float weight_decay, int64_t step, muon_stream_t stream);
+int muon_adamw_update_f32(float *param, const float *grad, float *exp_avg, float *exp_avg_sq, int64_t numel,
+                          float lr, float beta1, float beta2, float eps, float weight_decay, int64_t step,
+                          muon_stream_t stream);
 
 /* The default shape scale sqrt(max(1, rows/cols)). */
 float muon_default_scale(int64_t rows, int64_t cols);

@@ -53,11 +53,15 @@ SIGNATURES = {
     "muon_ns_workspace_bytes": (_SIZE, [_I64, _I64, _I64]),
     "muon_ns_batched_ws": (_INT, [_P, _I64, _I64, _I64, _INT, _P, _F, _P, _SIZE, _P]),
     "muon_ns_batched_static": (_INT, [_P, _I64, _I64, _I64, _INT, _P, _F, _P]),
+    "muon_ns_batched_schedule": (_INT, [_P, _I64, _I64, _I64, _INT, _P, _F, _P]),
+    "muon_ns_batched_schedule_f32": (_INT, [_P, _I64, _I64, _I64, _INT, _P, _F, _P]),
     "muon_ns_batched_f32": (_INT, [_P, _I64, _I64, _I64, _INT, _P, _F, _P]),
     "muon_ns_workspace_bytes_f32": (_SIZE, [_I64, _I64, _I64]),
     "muon_apply_update": (_INT, [_P, _P, _I64, _I64, _I64, _F, _F, _F, _P]),
     "muon_apply_update_f32": (_INT, [_P, _P, _I64, _I64, _I64, _F, _F, _F, _P]),
     "muon_default_scale": (_F, [_I64, _I64]),
+    "muon_adamw_update": (_INT, [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P]),
+    "muon_adamw_update_f32": (_INT, [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P]),
     "muon_get_device_status": (_INT, [_P]),
     "muon_status_string": (ctypes.c_char_p, [_INT]),
     "muon_set_wait_timeout_ns": (_U64, [_U64]),
@@ -204,6 +208,36 @@ def muon_ns_batched_static(X, steps=5, coeffs=QUINTIC, eps=1e-7, stream=None):
     return X
 
 
+def _schedule(coeff_rows):
+    rows = [tuple(float(v) for v in r) for r in coeff_rows]
+    if any(len(r) != 3 for r in rows):
+        raise ValueError("every schedule row must be (a, b, c)")
+    flat = [v for r in rows for v in r]
+    return len(rows), (ctypes.c_float * max(1, len(flat)))(*flat)
+
+
+def muon_ns_batched_schedule(X, coeff_rows, eps=1e-7, stream=None):
+    """Batched Newton-Schulz with one (a, b, c) row per step (bf16, in place)."""
+    import torch
+    _need(X, torch.bfloat16, "X")
+    b, m, n = _bmn(X)
+    steps, arr = _schedule(coeff_rows)
+    _check("muon_ns_batched_schedule", lib().muon_ns_batched_schedule(
+        _ptr(X), b, m, n, steps, arr, float(eps), _stream_handle(stream)))
+    return X
+
+
+def muon_ns_batched_schedule_f32(X, coeff_rows, eps=1e-7, stream=None):
+    """fp32 verification mode of muon_ns_batched_schedule (in place)."""
+    import torch
+    _need(X, torch.float32, "X")
+    b, m, n = _bmn(X)
+    steps, arr = _schedule(coeff_rows)
+    _check("muon_ns_batched_schedule_f32", lib().muon_ns_batched_schedule_f32(
+        _ptr(X), b, m, n, steps, arr, float(eps), _stream_handle(stream)))
+    return X
+
+
 def muon_ns_batched_f32(X, steps=5, coeffs=QUINTIC, eps=1e-7, stream=None):
     """fp32 verification mode of muon_ns_batched (in place)."""
     import torch
@@ -235,6 +269,33 @@ def muon_apply_update_f32(param, update, lr=0.02, weight_decay=0.1, scale=0.0, s
     b, r, c = _bmn(param)
     _check("muon_apply_update_f32", lib().muon_apply_update_f32(
         _ptr(param), _ptr(update), b, r, c, float(lr), float(weight_decay), float(scale), _stream_handle(stream)))
+
+
+def muon_adamw_update(param, grad, exp_avg, exp_avg_sq, step, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8,
+                      weight_decay=0.1, stream=None):
+    """AdamW on bf16 params/grads with fp32 moments (in place); see muon.h."""
+    import torch
+    _need(param, torch.bfloat16, "param")
+    _need(grad, torch.bfloat16, "grad")
+    _need(exp_avg, torch.float32, "exp_avg")
+    _need(exp_avg_sq, torch.float32, "exp_avg_sq")
+    if not (param.numel() == grad.numel() == exp_avg.numel() == exp_avg_sq.numel()):
+        raise ValueError("all AdamW tensors must have the same number of elements")
+    _check("muon_adamw_update", lib().muon_adamw_update(
+        _ptr(param), _ptr(grad), _ptr(exp_avg), _ptr(exp_avg_sq), param.numel(), float(lr), float(beta1),
+        float(beta2), float(eps), float(weight_decay), int(step), _stream_handle(stream)))
+
+
+def muon_adamw_update_f32(param, grad, exp_avg, exp_avg_sq, step, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8,
+                          weight_decay=0.1, stream=None):
+    import torch
+    for t, n in ((param, "param"), (grad, "grad"), (exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq")):
+        _need(t, torch.float32, n)
+    if not (param.numel() == grad.numel() == exp_avg.numel() == exp_avg_sq.numel()):
+        raise ValueError("all AdamW tensors must have the same number of elements")
+    _check("muon_adamw_update_f32", lib().muon_adamw_update_f32(
+        _ptr(param), _ptr(grad), _ptr(exp_avg), _ptr(exp_avg_sq), param.numel(), float(lr), float(beta1),
+        float(beta2), float(eps), float(weight_decay), int(step), _stream_handle(stream)))
 
 
 def muon_default_scale(rows, cols):

@@ -32,7 +32,7 @@ std::atomic<int64_t> g_launches{0};
 const char *kTraceNames[kTraceKinds] = {"momentum_bf16", "momentum_f32", "norm_partial", "norm_final",
                                         "transpose",     "scale",        "ns_syrk_tc",   "ns_poly_tc",
                                         "ns_axpy_tc",    "apply_bf16",   "apply_f32",    "gemm_f32",
-                                        "copy",          "selftest_wait"};
+                                        "copy",          "selftest_wait", "adamw"};
 
 struct TraceRec {
   int kind;
@@ -159,10 +159,13 @@ Workspace carve(void *base, int64_t batch, int64_t mm, int64_t nn, size_t elem) 
   return w;
 }
 
-int check_ns_args(const void *X, int64_t batch, int64_t m, int64_t n, int steps, const float *coeffs, float eps) {
+// ncoeff: how many floats `coeffs` holds (3, or 3 * steps for a schedule)
+int check_ns_args(const void *X, int64_t batch, int64_t m, int64_t n, int steps, const float *coeffs, float eps,
+                  int64_t ncoeff = 3) {
   if (batch < 0 || m < 1 || n < 1 || steps < 0 || !coeffs) return MUON_ERR_INVALID_ARG;
+  if (steps > 1000) return MUON_ERR_INVALID_ARG;
   if (!(eps >= 0.f) || !isfinite(eps)) return MUON_ERR_INVALID_ARG;
-  for (int i = 0; i < 3; ++i)
+  for (int64_t i = 0; i < ncoeff; ++i)
     if (!isfinite(coeffs[i])) return MUON_ERR_INVALID_ARG;
   if (batch > 0 && !X) return MUON_ERR_INVALID_ARG;
   if (m > (1 << 20) || n > (1 << 20) || batch > (int64_t(1) << 31)) return MUON_ERR_UNSUPPORTED;
@@ -186,8 +189,9 @@ int copy_async(void *dst, const void *src, size_t bytes, cudaStream_t s) {
 // matrix).  With `final_dst` set the result ends there (which may be src0
 // itself); with final_dst == nullptr it stays in whichever buffer the last
 // iteration wrote, returned through `result`.
+// cf holds (a, b, c) for step it at cf + it * cf_stride (stride 0: one triple).
 int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *final_dst, const Workspace &w, int64_t batch, int64_t mm,
-                 int64_t nn, bool transposed, int steps, const float *cf, float eps, cudaStream_t s,
+                 int64_t nn, bool transposed, int steps, const float *cf, int cf_stride, float eps, cudaStream_t s,
                  __nv_bfloat16 **result) {
   const int64_t per = mm * nn;
   MUON_TRY(launch_inv_norm_bf16(src0, batch, per, eps, w.partial, w.inv, w.inv2, s));
@@ -205,10 +209,11 @@ int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *final_dst, const Workspace 
     const bool last = it == steps - 1;
     __nv_bfloat16 *dst = (src == x1) ? x2 : x1;
     if (last && final_dst && final_dst != src) dst = final_dst;
+    const float *c = cf + (size_t)it * cf_stride;
     MUON_TRY(ns_syrk(src, A, batch, mm, nn, it == 0 ? w.inv2 : nullptr, transposed, s));
-    MUON_TRY(ns_poly(A, B, batch, mm, cf[1], cf[2], s));
+    MUON_TRY(ns_poly(A, B, batch, mm, c[1], c[2], s));
     // the input X is exactly bf16 (no low half); the result leaves as bf16
-    MUON_TRY(ns_axpy(B, src, it == 0 ? nullptr : lo, dst, last ? nullptr : lo, batch, mm, nn, cf[0],
+    MUON_TRY(ns_axpy(B, src, it == 0 ? nullptr : lo, dst, last ? nullptr : lo, batch, mm, nn, c[0],
                      it == 0 ? w.inv : nullptr, transposed, s));
     src = dst;
   }
@@ -221,7 +226,7 @@ int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *final_dst, const Workspace 
 }
 
 int ns_f32_core(float *src0, float *final_dst, const Workspace &w, int64_t batch, int64_t mm, int64_t nn, int steps,
-                const float *cf, float eps, cudaStream_t s, float **result) {
+                const float *cf, int cf_stride, float eps, cudaStream_t s, float **result) {
   const int64_t per = mm * nn;
   MUON_TRY(launch_inv_norm_f32(src0, batch, per, eps, w.partial, w.inv, w.inv2, s));
   auto *x1 = static_cast<float *>(w.x1);
@@ -237,9 +242,10 @@ int ns_f32_core(float *src0, float *final_dst, const Workspace &w, int64_t batch
     const bool last = it == steps - 1;
     float *dst = (src == x1) ? x2 : x1;
     if (last && final_dst && final_dst != src) dst = final_dst;
+    const float *c = cf + (size_t)it * cf_stride;
     MUON_TRY(gemm_f32(0, src, nullptr, A, batch, mm, nn, 0.f, 0.f, 0.f, it == 0 ? w.inv2 : nullptr, s));
-    MUON_TRY(gemm_f32(1, A, nullptr, B, batch, mm, mm, 0.f, cf[1], cf[2], nullptr, s));
-    MUON_TRY(gemm_f32(2, B, src, dst, batch, mm, nn, cf[0], 0.f, 0.f, it == 0 ? w.inv : nullptr, s));
+    MUON_TRY(gemm_f32(1, A, nullptr, B, batch, mm, mm, 0.f, c[1], c[2], nullptr, s));
+    MUON_TRY(gemm_f32(2, B, src, dst, batch, mm, nn, c[0], 0.f, 0.f, it == 0 ? w.inv : nullptr, s));
     src = dst;
   }
   if (final_dst && src != final_dst) {
@@ -248,6 +254,66 @@ int ns_f32_core(float *src0, float *final_dst, const Workspace &w, int64_t batch
   }
   *result = src;
   return MUON_OK;
+}
+
+// Checked arguments; X in caller layout.  For m > n the iteration runs on X^T
+// without moving data: the kernels read the stored matrix as the transpose of
+// the canonical mm x nn one.
+int ns_bf16_entry(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float *cf, int cf_stride, float eps,
+                  void *workspace, size_t workspace_bytes, cudaStream_t s) {
+  if (batch == 0) return MUON_OK;
+  if (m % 8 || n % 8 || !aligned16(X)) return MUON_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MUON_ERR_INVALID_ARG;
+  const int64_t mm = std::min(m, n), nn = std::max(m, n);
+  if (workspace_bytes < ws_bytes(batch, mm, nn, 2)) return MUON_ERR_NO_MEMORY;
+  if (!device_error_word()) return MUON_ERR_CUDA;
+  Workspace w = carve(workspace, batch, mm, nn, 2);
+  auto *x = static_cast<__nv_bfloat16 *>(X);
+  __nv_bfloat16 *res = nullptr;
+  return ns_bf16_core(x, x, w, batch, mm, nn, m > n, steps, cf, cf_stride, eps, s, &res);
+}
+
+// Allocates the workspace stream-ordered on s around ns_bf16_entry.
+int ns_bf16_alloc(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float *cf, int cf_stride, float eps,
+                  cudaStream_t s) {
+  if (batch == 0) return MUON_OK;
+  if (m % 8 || n % 8 || !aligned16(X)) return MUON_ERR_UNSUPPORTED;
+  const size_t bytes = ws_bytes(batch, std::min(m, n), std::max(m, n), 2);
+  void *ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess || !ws) {
+    cudaGetLastError();
+    return MUON_ERR_NO_MEMORY;
+  }
+  int st = ns_bf16_entry(X, batch, m, n, steps, cf, cf_stride, eps, ws, bytes, s);
+  cudaError_t fe = cudaFreeAsync(ws, s);
+  if (st == MUON_OK && fe != cudaSuccess) st = MUON_ERR_CUDA;
+  return st;
+}
+
+int ns_f32_alloc(float *X, int64_t batch, int64_t m, int64_t n, int steps, const float *cf, int cf_stride, float eps,
+                 cudaStream_t s) {
+  if (batch == 0) return MUON_OK;
+  const size_t bytes = ws_bytes(batch, std::min(m, n), std::max(m, n), 4);
+  void *ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess || !ws) {
+    cudaGetLastError();
+    return MUON_ERR_NO_MEMORY;
+  }
+  const int64_t mm = std::min(m, n), nn = std::max(m, n);
+  Workspace w = carve(ws, batch, mm, nn, 4);
+  int st;
+  float *res = nullptr;
+  if (m <= n) {
+    st = ns_f32_core(X, X, w, batch, mm, nn, steps, cf, cf_stride, eps, s, &res);
+  } else {
+    float *xt = static_cast<float *>(w.x1);
+    st = launch_transpose_f32(X, xt, batch, m, n, s);
+    if (st == MUON_OK) st = ns_f32_core(xt, nullptr, w, batch, mm, nn, steps, cf, cf_stride, eps, s, &res);
+    if (st == MUON_OK) st = launch_transpose_f32(res, X, batch, mm, nn, s);
+  }
+  cudaError_t fe = cudaFreeAsync(ws, s);
+  if (st == MUON_OK && fe != cudaSuccess) st = MUON_ERR_CUDA;
+  return st;
 }
 
 }  // namespace
@@ -289,67 +355,37 @@ size_t muon_ns_workspace_bytes_f32(int64_t batch, int64_t m, int64_t n) {
 int muon_ns_batched_ws(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3], float eps,
                        void *workspace, size_t workspace_bytes, muon_stream_t stream) {
   MUON_TRY(check_ns_args(X, batch, m, n, steps, coeffs, eps));
-  if (batch == 0) return MUON_OK;
-  if (m % 8 || n % 8 || !aligned16(X)) return MUON_ERR_UNSUPPORTED;
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MUON_ERR_INVALID_ARG;
-  if (workspace_bytes < muon_ns_workspace_bytes(batch, m, n)) return MUON_ERR_NO_MEMORY;
-  if (!device_error_word()) return MUON_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const float cf[3] = {coeffs[0], coeffs[1], coeffs[2]};
-  const int64_t mm = std::min(m, n), nn = std::max(m, n);
-  Workspace w = carve(workspace, batch, mm, nn, 2);
-  auto *x = static_cast<__nv_bfloat16 *>(X);
-  __nv_bfloat16 *res = nullptr;
-  // m > n: the iteration runs on X^T without moving data -- the kernels read
-  // the stored matrix as the transpose of the canonical mm x nn one
-  return ns_bf16_core(x, x, w, batch, mm, nn, m > n, steps, cf, eps, s, &res);
+  return ns_bf16_entry(X, batch, m, n, steps, cf, 0, eps, workspace, workspace_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 int muon_ns_batched(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3], float eps,
                     muon_stream_t stream) {
   MUON_TRY(check_ns_args(X, batch, m, n, steps, coeffs, eps));
-  if (batch == 0) return MUON_OK;
-  if (m % 8 || n % 8 || !aligned16(X)) return MUON_ERR_UNSUPPORTED;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t bytes = muon_ns_workspace_bytes(batch, m, n);
-  void *ws = nullptr;
-  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess || !ws) {
-    cudaGetLastError();
-    return MUON_ERR_NO_MEMORY;
-  }
-  int st = muon_ns_batched_ws(X, batch, m, n, steps, coeffs, eps, ws, bytes, stream);
-  cudaError_t fe = cudaFreeAsync(ws, s);
-  if (st == MUON_OK && fe != cudaSuccess) st = MUON_ERR_CUDA;
-  return st;
+  const float cf[3] = {coeffs[0], coeffs[1], coeffs[2]};
+  return ns_bf16_alloc(X, batch, m, n, steps, cf, 0, eps, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int muon_ns_batched_schedule(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float *coeffs,
+                             float eps, muon_stream_t stream) {
+  MUON_TRY(check_ns_args(X, batch, m, n, steps, coeffs, eps, 3 * (int64_t)steps));
+  std::vector<float> cf(coeffs, coeffs + 3 * (size_t)steps);
+  return ns_bf16_alloc(X, batch, m, n, steps, cf.data(), 3, eps, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int muon_ns_batched_f32(float *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3], float eps,
                         muon_stream_t stream) {
   MUON_TRY(check_ns_args(X, batch, m, n, steps, coeffs, eps));
-  if (batch == 0) return MUON_OK;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t bytes = muon_ns_workspace_bytes_f32(batch, m, n);
-  void *ws = nullptr;
-  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess || !ws) {
-    cudaGetLastError();
-    return MUON_ERR_NO_MEMORY;
-  }
   const float cf[3] = {coeffs[0], coeffs[1], coeffs[2]};
-  const int64_t mm = std::min(m, n), nn = std::max(m, n);
-  Workspace w = carve(ws, batch, mm, nn, 4);
-  int st;
-  float *res = nullptr;
-  if (m <= n) {
-    st = ns_f32_core(X, X, w, batch, mm, nn, steps, cf, eps, s, &res);
-  } else {
-    float *xt = static_cast<float *>(w.x1);
-    st = launch_transpose_f32(X, xt, batch, m, n, s);
-    if (st == MUON_OK) st = ns_f32_core(xt, nullptr, w, batch, mm, nn, steps, cf, eps, s, &res);
-    if (st == MUON_OK) st = launch_transpose_f32(res, X, batch, mm, nn, s);
-  }
-  cudaError_t fe = cudaFreeAsync(ws, s);
-  if (st == MUON_OK && fe != cudaSuccess) st = MUON_ERR_CUDA;
-  return st;
+  return ns_f32_alloc(X, batch, m, n, steps, cf, 0, eps, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int muon_ns_batched_schedule_f32(float *X, int64_t batch, int64_t m, int64_t n, int steps, const float *coeffs,
+                                 float eps, muon_stream_t stream) {
+  MUON_TRY(check_ns_args(X, batch, m, n, steps, coeffs, eps, 3 * (int64_t)steps));
+  std::vector<float> cf(coeffs, coeffs + 3 * (size_t)steps);
+  return ns_f32_alloc(X, batch, m, n, steps, cf.data(), 3, eps, reinterpret_cast<cudaStream_t>(stream));
 }
 
 float muon_default_scale(int64_t rows, int64_t cols) {
@@ -384,6 +420,45 @@ int muon_apply_update_f32(float *param, const float *update, int64_t batch, int6
   float kw, ko;
   update_constants(rows, cols, lr, weight_decay, scale, &kw, &ko);
   return launch_apply_f32(param, update, numel, kw, ko, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static int adamw_consts(float lr, float beta1, float beta2, float eps, float wd, int64_t step, AdamWConsts *k) {
+  if (step < 1 || !isfinite(lr) || !isfinite(eps) || !isfinite(wd) || !(beta1 >= 0.f && beta1 < 1.f) ||
+      !(beta2 >= 0.f && beta2 < 1.f) || !(eps >= 0.f))
+    return MUON_ERR_INVALID_ARG;
+  const double t = (double)step;
+  k->b1 = beta1;
+  k->c1 = (float)(1.0 - (double)beta1);
+  k->b2 = beta2;
+  k->c2 = (float)(1.0 - (double)beta2);
+  k->bc2 = (float)(1.0 - pow((double)beta2, t));
+  k->step_size = (float)((double)lr / (1.0 - pow((double)beta1, t)));
+  k->kw = (float)(1.0 - (double)lr * (double)wd);
+  k->eps = eps;
+  if (!(k->bc2 > 0.f) || !isfinite(k->step_size)) return MUON_ERR_INVALID_ARG;
+  return MUON_OK;
+}
+
+int muon_adamw_update(void *param, const void *grad, float *exp_avg, float *exp_avg_sq, int64_t numel, float lr,
+                      float beta1, float beta2, float eps, float weight_decay, int64_t step, muon_stream_t stream) {
+  if (numel < 0) return MUON_ERR_INVALID_ARG;
+  AdamWConsts k;
+  MUON_TRY(adamw_consts(lr, beta1, beta2, eps, weight_decay, step, &k));
+  if (numel == 0) return MUON_OK;
+  if (!param || !grad || !exp_avg || !exp_avg_sq) return MUON_ERR_INVALID_ARG;
+  return launch_adamw_bf16(static_cast<__nv_bfloat16 *>(param), static_cast<const __nv_bfloat16 *>(grad), exp_avg,
+                           exp_avg_sq, numel, k, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int muon_adamw_update_f32(float *param, const float *grad, float *exp_avg, float *exp_avg_sq, int64_t numel, float lr,
+                          float beta1, float beta2, float eps, float weight_decay, int64_t step,
+                          muon_stream_t stream) {
+  if (numel < 0) return MUON_ERR_INVALID_ARG;
+  AdamWConsts k;
+  MUON_TRY(adamw_consts(lr, beta1, beta2, eps, weight_decay, step, &k));
+  if (numel == 0) return MUON_OK;
+  if (!param || !grad || !exp_avg || !exp_avg_sq) return MUON_ERR_INVALID_ARG;
+  return launch_adamw_f32(param, grad, exp_avg, exp_avg_sq, numel, k, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int muon_get_device_status(muon_stream_t stream) {

@@ -29,6 +29,7 @@ enum TraceKind : int {
   kTraceGemmF32,
   kTraceCopy,
   kTraceSelftest,
+  kTraceAdamW,
   kTraceKinds
 };
 
@@ -49,6 +50,14 @@ int launch_momentum_f32(const float *g, float *buf, float *u, int64_t numel, flo
 int launch_apply_bf16(__nv_bfloat16 *w, const __nv_bfloat16 *o, int64_t numel, float kw, float ko,
                       cudaStream_t s);
 int launch_apply_f32(float *w, const float *o, int64_t numel, float kw, float ko, cudaStream_t s);
+// AdamW constants, formed in double on the host and rounded once to fp32
+struct AdamWConsts {
+  float b1, c1, b2, c2, bc2, step_size, kw, eps;
+};
+int launch_adamw_bf16(__nv_bfloat16 *w, const __nv_bfloat16 *g, float *m, float *v, int64_t numel,
+                      const AdamWConsts &k, cudaStream_t s);
+int launch_adamw_f32(float *w, const float *g, float *m, float *v, int64_t numel, const AdamWConsts &k,
+                     cudaStream_t s);
 // Per-matrix inverse norm: inv[b] = 1/(||X_b||_F + eps), inv2[b] = inv[b]^2.
 // `partial` holds batch*norm_partials() floats of scratch.
 int norm_partials();

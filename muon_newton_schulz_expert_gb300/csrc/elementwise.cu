@@ -1,5 +1,6 @@
 // HBM-bound kernels of the Muon step: momentum, parameter update, per-matrix
-// Frobenius norm, transpose and per-matrix scaling.
+// Frobenius norm, transpose and per-matrix scaling; and the AdamW update of
+// the parameters Muon does not take.
 //
 // Source of the operations: "Training a 1T-Parameter MoE on EU public
 // infrastructure with PyTorch and TorchTitan", section "FlexShard: Muon without
@@ -135,6 +136,64 @@ __global__ void apply_f32_kernel(float *__restrict__ w, const float *__restrict_
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < numel;
        i += (int64_t)gridDim.x * blockDim.x)
     w[i] = upd(kw, ko, w[i], o[i]);
+}
+
+// ---------------------------------------------------------------- AdamW
+// Routers and embeddings take AdamW (two fp32 states per parameter); every
+// fp32 operation is rounded separately in the order stated in muon.h.
+__device__ __forceinline__ void adamw_elem(const AdamWConsts &k, float &w, float g, float &m, float &v) {
+  m = __fadd_rn(__fmul_rn(k.b1, m), __fmul_rn(k.c1, g));
+  v = __fadd_rn(__fmul_rn(k.b2, v), __fmul_rn(k.c2, __fmul_rn(g, g)));
+  const float d = __fadd_rn(__fsqrt_rn(__fdiv_rn(v, k.bc2)), k.eps);
+  w = __fsub_rn(__fmul_rn(k.kw, w), __fmul_rn(k.step_size, __fdiv_rn(m, d)));
+}
+
+__global__ void adamw_bf16_vec(uint4 *__restrict__ w8, const uint4 *__restrict__ g8, float4 *__restrict__ m4,
+                               float4 *__restrict__ v4, int64_t nvec, AdamWConsts k) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
+    Bf16x8 w, g, r;
+    w.v = __ldcs(w8 + i);
+    g.v = __ldcs(g8 + i);
+    float4 m0 = __ldcs(m4 + 2 * i), m1 = __ldcs(m4 + 2 * i + 1), v0 = __ldcs(v4 + 2 * i), v1 = __ldcs(v4 + 2 * i + 1);
+    float mf[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float vf[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float2 wf = __bfloat1622float2(w.h[e]), gf = __bfloat1622float2(g.h[e]);
+      adamw_elem(k, wf.x, gf.x, mf[2 * e], vf[2 * e]);
+      adamw_elem(k, wf.y, gf.y, mf[2 * e + 1], vf[2 * e + 1]);
+      r.h[e] = __floats2bfloat162_rn(wf.x, wf.y);
+    }
+    __stcs(w8 + i, r.v);
+    __stcs(m4 + 2 * i, make_float4(mf[0], mf[1], mf[2], mf[3]));
+    __stcs(m4 + 2 * i + 1, make_float4(mf[4], mf[5], mf[6], mf[7]));
+    __stcs(v4 + 2 * i, make_float4(vf[0], vf[1], vf[2], vf[3]));
+    __stcs(v4 + 2 * i + 1, make_float4(vf[4], vf[5], vf[6], vf[7]));
+  }
+}
+
+__global__ void adamw_bf16_scalar(__nv_bfloat16 *__restrict__ w, const __nv_bfloat16 *__restrict__ g,
+                                  float *__restrict__ m, float *__restrict__ v, int64_t begin, int64_t numel,
+                                  AdamWConsts k) {
+  for (int64_t i = begin + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < numel;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float wf = __bfloat162float(w[i]), mf = m[i], vf = v[i];
+    adamw_elem(k, wf, __bfloat162float(g[i]), mf, vf);
+    w[i] = __float2bfloat16_rn(wf);
+    m[i] = mf;
+    v[i] = vf;
+  }
+}
+
+__global__ void adamw_f32_kernel(float *__restrict__ w, const float *__restrict__ g, float *__restrict__ m,
+                                 float *__restrict__ v, int64_t numel, AdamWConsts k) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < numel; i += (int64_t)gridDim.x * blockDim.x) {
+    float wf = w[i], mf = m[i], vf = v[i];
+    adamw_elem(k, wf, g[i], mf, vf);
+    w[i] = wf;
+    m[i] = mf;
+    v[i] = vf;
+  }
 }
 
 // ---------------------------------------------------------------- norm
@@ -327,6 +386,38 @@ int launch_apply_bf16(__nv_bfloat16 *w, const __nv_bfloat16 *o, int64_t numel, f
     return trace_after(kTraceApply, s);
   }
   return MUON_OK;
+}
+
+int launch_adamw_bf16(__nv_bfloat16 *w, const __nv_bfloat16 *g, float *m, float *v, int64_t numel,
+                      const AdamWConsts &k, cudaStream_t s) {
+  if (numel == 0) return MUON_OK;
+  int64_t done = 0;
+  if (aligned16(w) && aligned16(g) && aligned16(m) && aligned16(v)) {
+    int64_t nvec = numel / 8;
+    if (nvec > 0) {
+      trace_before(kTraceAdamW, s);
+      adamw_bf16_vec<<<grid_for(nvec), kThreads, 0, s>>>(reinterpret_cast<uint4 *>(w), reinterpret_cast<const uint4 *>(g),
+                                                         reinterpret_cast<float4 *>(m), reinterpret_cast<float4 *>(v),
+                                                         nvec, k);
+      int st = trace_after(kTraceAdamW, s);
+      if (st) return st;
+    }
+    done = nvec * 8;
+  }
+  if (done < numel) {
+    trace_before(kTraceAdamW, s);
+    adamw_bf16_scalar<<<grid_for(numel - done), kThreads, 0, s>>>(w, g, m, v, done, numel, k);
+    return trace_after(kTraceAdamW, s);
+  }
+  return MUON_OK;
+}
+
+int launch_adamw_f32(float *w, const float *g, float *m, float *v, int64_t numel, const AdamWConsts &k,
+                     cudaStream_t s) {
+  if (numel == 0) return MUON_OK;
+  trace_before(kTraceAdamW, s);
+  adamw_f32_kernel<<<grid_for(numel), kThreads, 0, s>>>(w, g, m, v, numel, k);
+  return trace_after(kTraceAdamW, s);
 }
 
 int launch_apply_f32(float *w, const float *o, int64_t numel, float kw, float ko, cudaStream_t s) {

@@ -11,6 +11,7 @@ from .muon_oracle import (  # noqa: F401
     bf16_bits,
     bf16_from_bits,
     bf16_round,
+    coefficient_rows,
     default_scale,
     frobenius_normalise,
     gram,

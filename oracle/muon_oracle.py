@@ -130,21 +130,32 @@ def axpy_update(X: np.ndarray, B: np.ndarray, a: float) -> np.ndarray:
     return a * X + B @ X
 
 
+def coefficient_rows(steps: int, coeffs):
+    """The (a, b, c) of each step: one triple for every step, or one row per step."""
+    arr = np.asarray(coeffs, dtype=np.float64)
+    if arr.shape == (3,):
+        return [tuple(arr)] * int(steps)
+    if arr.shape != (int(steps), 3):
+        raise ValueError("coeffs must be (a, b, c) or one (a, b, c) row per step")
+    return [tuple(r) for r in arr]
+
+
 def newton_schulz(G, steps: int = DEFAULT_STEPS, coeffs=QUINTIC, eps: float = DEFAULT_EPS) -> np.ndarray:
     """Orthogonalise one matrix G (rows x cols); returns fp64 in G's layout.
 
     FlexShard section: a few Newton-Schulz iterations act on the whole matrix
     (each rank owns complete expert matrices).  Orientation: work on G^T when
-    rows > cols, so that A = X X^T is the smaller Gram matrix.
+    rows > cols, so that A = X X^T is the smaller Gram matrix.  ``coeffs`` is
+    one (a, b, c) for every step or a schedule of one row per step.
     """
     G = np.asarray(G, dtype=np.float64)
     if G.ndim != 2:
         raise ValueError("newton_schulz takes one 2-D matrix")
+    rows = coefficient_rows(steps, coeffs)
     transposed = G.shape[0] > G.shape[1]
     X = G.T if transposed else G
     X = frobenius_normalise(X, eps)
-    a, b, c = (float(v) for v in coeffs)
-    for _ in range(int(steps)):
+    for a, b, c in rows:
         A = gram(X)
         B = poly(A, b, c)
         X = axpy_update(X, B, a)

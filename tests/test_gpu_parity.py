@@ -213,3 +213,44 @@ def test_ns_bf16_low_rank_and_ill_conditioned(mk, index):
     X = ((U * s.unsqueeze(0)) @ V.T).to(torch.bfloat16).unsqueeze(0).contiguous()
     got, want = run_bf16_ns(mk, X)
     assert rel_fro(got, want) < BF16_TOL
+
+
+# ----------------------------------------------------------------------------- coefficient schedules
+# Schedules whose composite scalar map stays positive and well conditioned on
+# (0, 1] (relative sensitivity <= ~10): a schedule whose map crosses zero has
+# unbounded relative sensitivity there, and no bf16 computation can meet a
+# relative tolerance on it.
+SCHEDULES = {
+    "quintic_then_cubic": [O.QUINTIC] * 5 + [O.CUBIC] * 3,
+    "varied": [O.QUINTIC, (3.0, -3.2, 1.2), O.QUINTIC, (2.0, -1.5, 0.5)],
+}
+
+
+@pytest.mark.parametrize("name", sorted(SCHEDULES))
+@pytest.mark.parametrize("count,m,n", [(3, 256, 768), (2, 640, 200)])
+def test_ns_schedule_bf16_matches_oracle(mk, name, count, m, n):
+    rows = SCHEDULES[name]
+    X = workloads.gradients(count, m, n, 5000 + m, device="cuda")
+    x_in = np32(X)
+    mk.muon_ns_batched_schedule(X, rows)
+    assert mk.muon_get_device_status() == 0
+    want = O.newton_schulz_batched(x_in, len(rows), rows)
+    assert rel_fro(np32(X), want) < BF16_TOL
+
+
+@pytest.mark.parametrize("name", sorted(SCHEDULES))
+def test_ns_schedule_f32_matches_oracle(mk, name):
+    rows = SCHEDULES[name]
+    gen = torch.Generator("cuda").manual_seed(77)
+    X = torch.randn(4, 48, 96, generator=gen, device="cuda")
+    want = O.newton_schulz_batched(np32(X), len(rows), rows)
+    mk.muon_ns_batched_schedule_f32(X, rows)
+    assert rel_fro(np32(X), want) < F32_TOL
+
+
+def test_ns_schedule_of_equal_rows_is_the_constant_call(mk):
+    X = workloads.gradients(2, 128, 512, 91, device="cuda")
+    Y = X.clone()
+    mk.muon_ns_batched(X, steps=5)
+    mk.muon_ns_batched_schedule(Y, [O.QUINTIC] * 5)
+    assert torch.equal(X, Y)

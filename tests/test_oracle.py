@@ -397,3 +397,53 @@ def test_workload_shapes_follow_the_pages():
     shapes = {(g.rows, g.cols) for g in c3.groups}
     assert shapes == {(facts["hidden"], facts["expert_hidden"]), (facts["expert_hidden"], facts["hidden"])}
     assert sum(g.count for g in c3.groups) == 96   # 32 experts x (w1, w3, w2)
+
+
+# --------------------------------------------------------------------------
+# coefficient schedules (one (a, b, c) per step)
+# --------------------------------------------------------------------------
+def schedule_map(s, rows):
+    s = np.asarray(s, np.float64)
+    for a, b, c in rows:
+        s = a * s + b * s ** 3 + c * s ** 5
+    return s
+
+
+def test_schedule_matches_svd_closed_form():
+    rng = np.random.default_rng(30)
+    rows = [(4.0, -5.0, 2.0), (3.4445, -4.7750, 2.0315), (2.0, -1.5, 0.5), (1.5, -0.5, 0.0)]
+    for m, n in [(16, 48), (48, 16), (24, 24)]:
+        G = rng.standard_normal((m, n))
+        got = O.newton_schulz(G, len(rows), rows, 1e-7)
+        U, S, Vt = np.linalg.svd(G, full_matrices=False)
+        want = (U * schedule_map(S / (math.sqrt(float(np.sum(S * S))) + 1e-7), rows)) @ Vt
+        assert rel_fro(got, want) < 1e-10
+
+
+def test_schedule_of_identical_rows_equals_constant_coefficients():
+    rng = np.random.default_rng(31)
+    G = rng.standard_normal((20, 60))
+    assert np.array_equal(O.newton_schulz(G, 5, [O.QUINTIC] * 5), O.newton_schulz(G, 5, O.QUINTIC))
+
+
+def test_schedule_order_matters():
+    # the step maps do not commute in general: reversing the schedule changes the result
+    rng = np.random.default_rng(32)
+    G = rng.standard_normal((16, 40))
+    rows = [(3.4445, -4.7750, 2.0315), (1.5, -0.5, 0.0), (2.0, -1.5, 0.5)]
+    assert rel_fro(O.newton_schulz(G, 3, rows), O.newton_schulz(G, 3, rows[::-1])) > 1e-3
+
+
+def test_quintic_then_cubic_reaches_polar_factor():
+    rng = np.random.default_rng(33)
+    U = haar(16, rng)
+    V = haar(48, rng)[:, :16]
+    s = np.exp(rng.uniform(math.log(1e-2), 0, 16))
+    G = (U * s) @ V.T
+    rows = [O.QUINTIC] * 5 + [O.CUBIC] * 12
+    assert rel_fro(O.newton_schulz(G, len(rows), rows), U @ V.T) < 1e-10
+
+
+def test_schedule_shape_is_checked():
+    with pytest.raises(ValueError):
+        O.newton_schulz(np.ones((4, 8)), 3, [O.QUINTIC] * 2)
