@@ -304,6 +304,9 @@ def run_gpu(args):
                "h2d_bytes_per_step": numel * 2, "d2h_bytes_per_step": numel * 2, "steps": ke,
                "copies": "pinned host, side streams overlapped with compute"}
 
+    host_res = None if args.no_host_resident else bench_host_resident(mk, torch, dev, stream, params, grads[0],
+                                                                          groups, split, total, world, dist,
+                                                                          max(3, args.steps // 3))
     peaks, peak_src = load_peaks()
     adamw = None if args.no_adamw else bench_adamw(mk, torch, dev, stream, float(peaks.get("hbm_gbs", 6800.0)))
     kernels = {}
@@ -351,7 +354,7 @@ def run_gpu(args):
         "tensor_kernels_tflops": round(total * FLOPS_NS / (tc_ms / 1e3) / 1e12, 1) if tc_ms else None,
         "flops_per_matrix": {"algorithmic_symmetric": FLOPS_NS, "dense_equivalent": FLOPS_NS_DENSE},
         "roofline": roof, "kernels": kernels, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
-        "adamw": adamw,
+        "adamw": adamw, "host_resident": host_res,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -359,6 +362,38 @@ def run_gpu(args):
         print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def bench_host_resident(mk, torch, dev, stream, params, grads, groups, split, total, world, dist, steps):
+    """The step with parameters, gradients and momentum in pinned host memory
+    (the pages' CPU-offload setting), streamed through the GPU by
+    muon_step_host: 8 bytes per element in (bf16 gradient and parameter, fp32
+    momentum) and 6 out (parameter and momentum) every step."""
+    numel = params.numel()
+    ph = params.cpu().pin_memory()
+    gh = grads.cpu().pin_memory()
+    mh = torch.zeros(numel, dtype=torch.float32).pin_memory()
+    p_views, g_views, m_views = split(ph), split(gh), split(mh)
+
+    def one():
+        for pv, gv, mv in zip(p_views, g_views, m_views):
+            mk.muon_step_host(pv, gv, mv, mu=MU, steps=5, coeffs=QUINTIC, eps=EPS, lr=LR, weight_decay=WD,
+                              chunk=8, stream=stream)
+
+    one()
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1) / steps)
+    del ph, gh, mh
+    return {"value": round(aggregate_value(total, world, ms), 3), "unit": UNIT, "ms_per_step": round(ms, 3),
+            "steps": steps, "h2d_bytes_per_step": numel * 8, "d2h_bytes_per_step": numel * 6, "chunk": 8,
+            "api": "muon_step_host (pinned host parameters, gradients and momentum)"}
 
 
 def bench_adamw(mk, torch, dev, stream, hbm_peak, steps=10, warmup=3):
@@ -471,6 +506,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-adamw", action="store_true", help="skip the AdamW (routers/embeddings) measurement")
+    ap.add_argument("--no-host-resident", action="store_true", help="skip the host-resident state measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="rank96", choices=["rank96", "profile8"],
                     help="rank96: the 96-matrix bench workload; profile8: 8 matrices for ncu captures")

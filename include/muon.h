@@ -169,6 +169,28 @@ int muon_apply_update_f32(float *param, const float *update, int64_t batch, int6
                           float lr, float weight_decay, float scale, muon_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The whole Muon step on matrices that live in host memory (FlexShard
+ * section: with the parameters offloaded to host memory, Newton-Schulz runs on
+ * the GPU).  param_host (bf16, in/out), grad_host (bf16) and momentum_host
+ * (fp32, in/out) are page-locked host arrays (cudaHostAlloc /
+ * cudaHostRegister) of batch matrices rows x cols.  The batch is streamed
+ * through the GPU `chunk` matrices at a time (0: 8) in two device slots:
+ * copies in and out run on two internal streams and overlap the compute of
+ * the neighbouring chunk, which runs on `stream` and is exactly
+ * muon_momentum_update -> muon_ns_batched -> muon_apply_update.  The call
+ * returns once the work is enqueued; when `stream` reaches it, the host
+ * arrays hold the updated parameters and momentum (do not touch them before).
+ * Device memory (2 slots of 14 bytes per element plus one Newton-Schulz
+ * workspace of `chunk` matrices) is allocated and freed stream-ordered on
+ * `stream`.  Errors: MUON_ERR_INVALID_ARG for bad sizes or null pointers,
+ * MUON_ERR_UNSUPPORTED for rows or cols not multiples of 8 or pageable host
+ * memory, MUON_ERR_NO_MEMORY, MUON_ERR_CUDA.
+ */
+int muon_step_host(void *param_host, const void *grad_host, float *momentum_host, int64_t batch, int64_t rows,
+                   int64_t cols, float mu, int nesterov, int steps, const float coeffs[3], float eps, float lr,
+                   float weight_decay, float scale, int64_t chunk, muon_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * AdamW for the parameters Muon does not take (FlexShard section: routers and
  * embeddings use AdamW, with two fp32 states per parameter).  Reading taken:
  * decoupled weight decay with bias correction, every fp32 operation rounded

@@ -60,6 +60,7 @@ SIGNATURES = {
     "muon_apply_update": (_INT, [_P, _P, _I64, _I64, _I64, _F, _F, _F, _P]),
     "muon_apply_update_f32": (_INT, [_P, _P, _I64, _I64, _I64, _F, _F, _F, _P]),
     "muon_default_scale": (_F, [_I64, _I64]),
+    "muon_step_host": (_INT, [_P, _P, _P, _I64, _I64, _I64, _F, _INT, _INT, _P, _F, _F, _F, _F, _I64, _P]),
     "muon_adamw_update": (_INT, [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P]),
     "muon_adamw_update_f32": (_INT, [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P]),
     "muon_get_device_status": (_INT, [_P]),
@@ -296,6 +297,25 @@ def muon_adamw_update_f32(param, grad, exp_avg, exp_avg_sq, step, lr=1e-3, beta1
     _check("muon_adamw_update_f32", lib().muon_adamw_update_f32(
         _ptr(param), _ptr(grad), _ptr(exp_avg), _ptr(exp_avg_sq), param.numel(), float(lr), float(beta1),
         float(beta2), float(eps), float(weight_decay), int(step), _stream_handle(stream)))
+
+
+def muon_step_host(param_host, grad_host, momentum_host, *, mu=0.95, nesterov=True, steps=5, coeffs=QUINTIC,
+                   eps=1e-7, lr=0.02, weight_decay=0.1, scale=0.0, chunk=0, stream=None):
+    """One Muon step on pinned host tensors (batch, rows, cols), streamed through the GPU."""
+    import torch
+    for t, n, dt in ((param_host, "param_host", torch.bfloat16), (grad_host, "grad_host", torch.bfloat16),
+                     (momentum_host, "momentum_host", torch.float32)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise TypeError(f"{n} must be a contiguous host {dt} tensor")
+        if not t.is_pinned():
+            raise ValueError(f"{n} must be in page-locked (pinned) host memory")
+    if not (param_host.shape == grad_host.shape == momentum_host.shape):
+        raise ValueError("param, grad and momentum must have the same shape")
+    b, r, c = _bmn(param_host)
+    _check("muon_step_host", lib().muon_step_host(
+        _ptr(param_host), _ptr(grad_host), _ptr(momentum_host), b, r, c, float(mu), int(bool(nesterov)), int(steps),
+        _coeffs(coeffs), float(eps), float(lr), float(weight_decay), float(scale), int(chunk),
+        _stream_handle(stream)))
 
 
 def muon_default_scale(rows, cols):

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmuon.so")
-SOURCES = ["api.cu", "elementwise.cu", "gemm_tc.cu", "gemm_f32.cu", "ns_static.cu"]
+SOURCES = ["api.cu", "elementwise.cu", "gemm_tc.cu", "gemm_f32.cu", "ns_static.cu", "host_stream.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 
