@@ -69,7 +69,7 @@ constexpr int UMMA_K = 16;
 #define MUON_SLOTS_POLY 2
 #endif
 #ifndef MUON_STAGES_AXPY
-#define MUON_STAGES_AXPY 5
+#define MUON_STAGES_AXPY 4
 #endif
 #ifndef MUON_SLOTS_AXPY
 #define MUON_SLOTS_AXPY 2
@@ -95,7 +95,10 @@ struct Layout {
   static constexpr int stages =
       EPI == EPI_AXPY ? MUON_STAGES_AXPY : (EPI == EPI_POLY ? MUON_STAGES_POLY : MUON_STAGES_SYRK);
   static constexpr int slots = EPI == EPI_AXPY ? MUON_SLOTS_AXPY : (EPI == EPI_POLY ? MUON_SLOTS_POLY : MUON_SLOTS_SYRK);
-  static constexpr int epi_bytes = EPI_WARPS * slots * EPI_BUF;
+  // AXPY stages its output in a box of its own, so that fetching the next
+  // input never waits for the previous store to finish reading.
+  static constexpr int out_slots = EPI == EPI_AXPY ? 1 : 0;
+  static constexpr int epi_bytes = EPI_WARPS * (slots + out_slots) * EPI_BUF;
   static constexpr int num_bars = 2 * stages + 5 + EPI_WARPS * slots;
   static constexpr int smem_bytes = stages * STAGE_BYTES + epi_bytes + 1024 + num_bars * 8 + 16;
   static_assert(CHUNKS % slots == 0, "chunks per tile must fill the staging slots evenly");
@@ -492,8 +495,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int SLOTS = Layout<EPI>::slots;
     const int ew = warp - 2;
     const int q = warp & 3, half = ew >> 2;
-    uint8_t *ebase = epi_smem + ew * SLOTS * EPI_BUF;   // slots of [hi box][lo box]
+    // SLOTS input slots of [hi box][lo box], then the output slot
+    uint8_t *ebase = epi_smem + ew * (SLOTS + 1) * EPI_BUF;
     const uint32_t ebase_s = smem_u32(ebase);
+    uint8_t *obuf = ebase + SLOTS * EPI_BUF;
+    const uint32_t obuf_s = ebase_s + SLOTS * EPI_BUF;
     uint32_t ephase_bits = 0;                                // parity per slot
     const bool lo_in = p.src_lo != nullptr, lo_out = p.out_lo != nullptr;
     const uint32_t etx = lo_in ? 2u * EPI_BOX_BYTES : (uint32_t)EPI_BOX_BYTES;
@@ -539,6 +545,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t r[32];
         __syncwarp();
         tmem_ld32(taddr + (uint32_t)(ch * 32), r);
+        if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the output box
+        __syncwarp();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint32_t off = (uint32_t)(lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
@@ -555,18 +563,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float2 hh = __bfloat1622float2(ho.h[e]);
             lo.h[e] = __floats2bfloat162_rn(v0 - hh.x, v1 - hh.y);
           }
-          *reinterpret_cast<uint4 *>(ebuf + off) = ho.v;
-          if (lo_out) *reinterpret_cast<uint4 *>(ebuf + EPI_BOX_BYTES + off) = lo.v;
+          *reinterpret_cast<uint4 *>(obuf + off) = ho.v;
+          if (lo_out) *reinterpret_cast<uint4 *>(obuf + EPI_BOX_BYTES + off) = lo.v;
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          const uint32_t src = ebase_s + slot * EPI_BUF;
-          tma_store_3d(&p.tm_out, src, col0, row0, mat);
-          if (lo_out) tma_store_3d(&p.tm_out_lo, src + EPI_BOX_BYTES, col0, row0, mat);
+          tma_store_3d(&p.tm_out, obuf_s, col0, row0, mat);
+          if (lo_out) tma_store_3d(&p.tm_out_lo, obuf_s + EPI_BOX_BYTES, col0, row0, mat);
           bulk_commit();
-          bulk_wait_read_all();
-          // this slot is free again: fetch chunk ch + SLOTS (possibly of the next tile)
+          // every lane has read this input slot: fetch chunk ch + SLOTS into it (possibly of the next tile)
           const int nc = ch + SLOTS;
           if (nc < CHUNKS)
             epi_load(slot, mat, row0, col0 + SLOTS * 32);
