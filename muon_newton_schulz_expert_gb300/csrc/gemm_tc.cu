@@ -22,16 +22,19 @@
 // tcgen05.mma.cta_group::2 (M=256, N=256, K=16, bf16 in, fp32 accumulate):
 // each CTA holds 128 rows of A and a 128-row half of B in its own shared
 // memory, and each CTA's TMEM receives its 128 rows of the accumulator.  Per
-// SM this reads half the B bytes of a single-CTA 128 x 256 tile, which is what
-// keeps shared-memory bandwidth below the tensor cores' appetite.
+// SM this moves half the B bytes of a single-CTA 128 x 256 tile through
+// shared memory, which is what keeps its bandwidth below the tensor cores'
+// appetite.
 //   warp 0 lane 0  TMA producer (both CTAs): 128x64 bf16 boxes, 128-byte
-//                  swizzle, 6-stage ring; completion is signalled on the even
-//                  CTA's "full" barrier, which waits for both halves;
+//                  swizzle, a ring of 4-6 stages (Layout); completion is
+//                  signalled on the even CTA's "full" barrier, which counts
+//                  the bytes of both halves;
 //   warp 1         TMEM allocation of 512 columns (two 128 x 256 fp32
 //                  accumulators) in both CTAs; lane 0 of the even CTA issues
 //                  the MMAs and multicasts tcgen05.commit to both CTAs;
 //   warps 2..9     epilogue (both CTAs): warp w reads TMEM lanes
-//                  32*(w%4)..+31 and one 128-column half of the tile.
+//                  32*(w%4)..+31 and one 128-column half of the tile, and
+//                  moves 32 x 32 boxes through shared memory with TMA.
 // The double-buffered accumulator lets the epilogue of tile t overlap the
 // main loop of tile t+1.  Every mbarrier wait is bounded: when it runs out the
 // kernel records a timeout in the device error word, raises a shared abort

@@ -109,3 +109,32 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(mk, "_lib", None)
     with pytest.raises(mk.MuonLibraryMissing):
         mk.lib()
+
+
+def test_newer_entry_points_reject_bad_arguments_on_the_host(lib):
+    c3 = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+    # schedules: every coefficient checked, steps bounded
+    sched = (ctypes.c_float * 6)(3.4445, -4.775, 2.0315, float("nan"), 0, 0)
+    assert lib.muon_ns_batched_schedule(ctypes.c_void_p(256), 1, 8, 8, 2, sched, 1e-7, None) == -1
+    assert lib.muon_ns_batched_schedule(ctypes.c_void_p(256), 1, 12, 8, 1, sched, 1e-7, None) == -2
+    assert lib.muon_ns_batched_schedule(None, 0, 8, 8, 2, sched, 1e-7, None) == -1
+    assert lib.muon_ns_batched_schedule(ctypes.c_void_p(256), 1, 8, 8, 1001, c3, 1e-7, None) == -1
+    assert lib.muon_ns_batched_schedule_f32(None, 0, 3, 5, 1, c3, 1e-7, None) == 0
+    # AdamW: step >= 1, betas in [0, 1)
+    assert lib.muon_adamw_update(None, None, None, None, 0, 1e-3, 0.9, 0.95, 1e-8, 0.1, 0, None) == -1
+    assert lib.muon_adamw_update(None, None, None, None, 0, 1e-3, 1.0, 0.95, 1e-8, 0.1, 1, None) == -1
+    assert lib.muon_adamw_update(None, None, None, None, 0, 1e-3, 0.9, 0.95, -1.0, 0.1, 1, None) == -1
+    assert lib.muon_adamw_update(None, None, None, None, 0, 1e-3, 0.9, 0.95, 1e-8, 0.1, 1, None) == 0
+    assert lib.muon_adamw_update(None, None, None, None, 16, 1e-3, 0.9, 0.95, 1e-8, 0.1, 1, None) == -1
+    assert lib.muon_adamw_update_f32(None, None, None, None, -1, 1e-3, 0.9, 0.95, 1e-8, 0.1, 1, None) == -1
+    # host-resident step: sizes, null pointers, shapes
+    assert lib.muon_step_host(None, None, None, 0, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, 0, None) == 0
+    assert lib.muon_step_host(None, None, None, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, 0, None) == -1
+    assert lib.muon_step_host(None, None, None, -1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, 0, None) == -1
+    assert lib.muon_step_host(None, None, None, 1, 8, 8, 0.95, 1, 5, None, 1e-7, 0.02, 0.1, 0.0, 0, None) == -1
+
+
+def test_trace_without_gpu_work_is_empty(lib):
+    assert lib.muon_trace_begin() == 0
+    entries = (mk.TraceEntry * 4)()
+    assert lib.muon_trace_end(entries, 4) == 0
