@@ -5,8 +5,11 @@ Workload (per GPU): 32 experts of the model-configuration table of "Training a
 (hidden 6144, expert hidden 1792): 64 matrices stored 6144 x 1792 (w1, w3) and
 32 stored 1792 x 6144 (w2), bf16 gradients N(0,1) times a per-row log-normal
 factor, fp32 momentum, bf16 parameters.  One step = momentum over all 96
-matrices, one batched Newton-Schulz call per stored shape (5 quintic steps),
-and the parameter update: the whole path.  Each rank owns whole matrices
+matrices, the batched Newton-Schulz iteration per stored shape (5 quintic
+steps) and the parameter update: the whole path.  By default each shape group
+is one fused call (muon_step_batched: momentum with the norm's sum of squares,
+then the iterations, the last of which writes the updated parameters);
+``--path unfused`` times the three separate calls instead.  Each rank owns whole matrices
 (section "FlexShard: Muon without communication"), so ranks share nothing and
 the scaling is weak: N GPUs process N x 96 matrices per step.
 
@@ -42,10 +45,11 @@ FLOPS_POLY = M_EXP ** 3
 FLOPS_AXPY = 2 * M_EXP * M_EXP * N_EXP
 FLOPS_NS = 5 * (FLOPS_SYRK + FLOPS_POLY + FLOPS_AXPY)        # 3.247e11
 FLOPS_NS_DENSE = 5 * (4 * M_EXP * M_EXP * N_EXP + 2 * M_EXP ** 3)
-KERNEL_FLOPS = {"ns_syrk_tc": FLOPS_SYRK, "ns_poly_tc": FLOPS_POLY, "ns_axpy_tc": FLOPS_AXPY}
+KERNEL_FLOPS = {"ns_syrk_tc": FLOPS_SYRK, "ns_poly_tc": FLOPS_POLY, "ns_axpy_tc": FLOPS_AXPY,
+                "ns_axpy_apply_tc": FLOPS_AXPY}
 PER_MATRIX_ELEMS = M_EXP * N_EXP
 # algorithmic HBM bytes per element of the elementwise kernels
-KERNEL_BYTES = {"momentum_bf16": 12, "apply_bf16": 6, "norm_partial": 2, "transpose": 4}
+KERNEL_BYTES = {"momentum_bf16": 12, "momentum_norm_bf16": 12, "apply_bf16": 6, "norm_partial": 2, "transpose": 4}
 
 
 def dist_env():
@@ -212,11 +216,25 @@ def run_gpu(args):
             v.copy_(workloads.gradients(c, r, k, seed0 + 100000 * s + 10 * i, device=dev))
         grads.append(g)
     momentum = torch.zeros(numel, dtype=torch.float32, device=dev)
-    upd = torch.empty(numel, dtype=torch.bfloat16, device=dev)
-    p_views, u_views = split(params), split(upd)
+    fused = args.path == "fused"
+    upd = None if fused else torch.empty(numel, dtype=torch.bfloat16, device=dev)
+    p_views, m_views = split(params), split(momentum)
+    g_views = [split(g) for g in grads]
+    u_views = None if fused else split(upd)
+    # one workspace, sized for the largest group, serves every fused call (all on one stream)
+    ws = torch.empty(max(mk.muon_step_workspace_bytes(c, r, k) for c, r, k in groups), dtype=torch.uint8,
+                     device=dev) if fused else None
     stream = torch.cuda.current_stream(dev)
 
+    def fused_group(p, g, m):
+        mk.muon_step_batched(p, g, m, mu=MU, nesterov=True, steps=5, coeffs=QUINTIC, eps=EPS, lr=LR,
+                             weight_decay=WD, scale=0.0, workspace=ws, stream=stream)
+
     def step(k):
+        if fused:
+            for p, g, m in zip(p_views, g_views[k % 2], m_views):
+                fused_group(p, g, m)
+            return
         mk.muon_momentum_update(grads[k % 2], momentum, upd, MU, True, stream)
         for u in u_views:
             mk.muon_ns_batched(u, 5, QUINTIC, EPS, stream)
@@ -263,7 +281,44 @@ def run_gpu(args):
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         g_dev = grads[0]
 
-        def e2e_steps(n):
+        host_p_views = split(host_p)
+
+        def e2e_steps_fused(n):
+            # step k's gradients arrive in device buffer k % 2, copied in while
+            # step k-1 computes; group j's parameters are copied out while the
+            # next group computes, and step k+1's call for group j (which
+            # writes its parameters) waits for that copy
+            ev_in, ev_used, ev_out = [None, None], [None, None], [None] * len(groups)
+
+            def copy_in(k):
+                i = k % 2
+                if ev_used[i] is not None:
+                    s_in.wait_event(ev_used[i])
+                else:
+                    s_in.wait_stream(stream)
+                with torch.cuda.stream(s_in):
+                    grads[i].copy_(host_g, non_blocking=True)
+                ev_in[i] = s_in.record_event()
+
+            copy_in(0)
+            for k in range(n):
+                i = k % 2
+                if k + 1 < n:
+                    copy_in(k + 1)
+                stream.wait_event(ev_in[i])
+                for j, (p, g, m) in enumerate(zip(p_views, g_views[i], m_views)):
+                    if ev_out[j] is not None:
+                        stream.wait_event(ev_out[j])
+                    fused_group(p, g, m)
+                    s_out.wait_event(stream.record_event())
+                    with torch.cuda.stream(s_out):
+                        host_p_views[j].copy_(p, non_blocking=True)
+                    ev_out[j] = s_out.record_event()
+                ev_used[i] = stream.record_event()
+            for e in ev_out:
+                stream.wait_event(e)
+
+        def e2e_steps_unfused(n):
             s_in.wait_stream(stream)
             with torch.cuda.stream(s_in):
                 g_dev.copy_(host_g, non_blocking=True)
@@ -290,6 +345,7 @@ def run_gpu(args):
                 ev_out = s_out.record_event()
             stream.wait_event(ev_out)
 
+        e2e_steps = e2e_steps_fused if fused else e2e_steps_unfused
         e2e_steps(2)
         torch.cuda.synchronize(dev)
         barrier(dist)
@@ -312,8 +368,8 @@ def run_gpu(args):
     kernels = {}
     for name, (n, t) in sorted(trace.items()):
         ent = {"launches": n, "avg_ms": round(t / n, 4), "share": None}
-        if name in KERNEL_FLOPS:   # every matrix passes through each tensor kernel 5 times per step
-            flops = KERNEL_FLOPS[name] * 5 * total * args.steps
+        if name in KERNEL_FLOPS:   # each launch covers one shape group
+            flops = KERNEL_FLOPS[name] * n * total / len(groups)
             ent["tflops"] = round(flops / (t / 1e3) / 1e12, 1)
         if name in KERNEL_BYTES:
             passes = 2 if name == "transpose" else 1
@@ -324,11 +380,11 @@ def run_gpu(args):
     traced_ms = sum(t for _, t in trace.values())
     for name, (n, t) in trace.items():
         kernels[name]["share"] = round(t / traced_ms, 4) if traced_ms else None
-    ns_ms = sum(trace.get(k, (0, 0.0))[1] for k in ("ns_syrk_tc", "ns_poly_tc", "ns_axpy_tc", "norm_partial",
-                                                        "norm_final", "transpose")) / args.steps
+    ns_ms = sum(trace.get(k, (0, 0.0))[1] for k in ("ns_syrk_tc", "ns_poly_tc", "ns_axpy_tc", "ns_axpy_apply_tc",
+                                                        "norm_partial", "norm_final", "transpose")) / args.steps
     dom = max(KERNEL_FLOPS, key=lambda k: trace.get(k, (0, 0.0))[1])
     dn, dt = trace[dom]
-    achieved = KERNEL_FLOPS[dom] * 5 * total * args.steps / (dt / 1e3) / 1e12
+    achieved = KERNEL_FLOPS[dom] * dn * total / len(groups) / (dt / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     traffic = args.traffic
     if traffic is None and dom == "ns_axpy_tc" and axpy_traffic_per_matrix():
@@ -347,6 +403,8 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD if args.workload == "rank96" else
                    "profile8: 8 x 1792x6144 bf16 (ncu capture case, not a bench line)", "matrices_per_gpu": total, "ns_steps": 5, "coeffs": list(QUINTIC),
                    "mu": MU, "lr": LR, "weight_decay": WD, "eps": EPS,
+                   "step_path": ("fused: muon_step_batched per shape group" if fused else
+                                 "unfused: momentum, muon_ns_batched per shape group, update"),
                    "l2": "inputs larger than L2 (2.1 GB bf16 gradients + 4.2 GB fp32 momentum per step)",
                    "parallelism": f"whole-matrix ownership, {world} independent replica(s), no collective"},
         "ns_tflops": round(total * FLOPS_NS / (ns_ms / 1e3) / 1e12, 1) if ns_ms else None,
@@ -510,6 +568,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="rank96", choices=["rank96", "profile8"],
                     help="rank96: the 96-matrix bench workload; profile8: 8 matrices for ncu captures")
+    ap.add_argument("--path", default="fused", choices=["fused", "unfused"],
+                    help="fused: one muon_step_batched call per shape group; unfused: the three separate calls")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture, if current")
     args = ap.parse_args()

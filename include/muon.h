@@ -169,6 +169,37 @@ int muon_apply_update_f32(float *param, const float *update, int64_t batch, int6
                           float lr, float weight_decay, float scale, muon_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The whole Muon step on matrices in device memory, fused (FlexShard section:
+ * momentum, Newton-Schulz on each whole matrix and the update, with no
+ * communication).  Computes, bit for bit, what
+ *   muon_momentum_update(grad, momentum, u, batch*rows*cols, mu, nesterov, s);
+ *   muon_ns_batched(u, batch, rows, cols, steps, coeffs, eps, s);
+ *   muon_apply_update(param, u, batch, rows, cols, lr, weight_decay, scale, s);
+ * compute, with no u array of the caller's and two passes over memory fewer:
+ * the momentum kernel also sums the squares of u for the Frobenius norm, and
+ * the last Newton-Schulz iteration applies the update to `param` in its
+ * epilogue instead of storing O.
+ *   param      device, bf16, [batch][rows][cols], read and written in place
+ *   grad       device, bf16, same layout (read)
+ *   momentum   device, fp32, same layout (read and written in place)
+ *   steps, coeffs, eps   as muon_ns_batched;  lr, weight_decay, scale as
+ *              muon_apply_update;  mu, nesterov as muon_momentum_update
+ *   workspace  device, 256-byte aligned, at least
+ *              muon_step_workspace_bytes(batch, rows, cols) bytes, used until
+ *              the enqueued work has finished; NULL (with any workspace_bytes)
+ *              allocates and frees it stream-ordered on `stream`
+ * The four arrays must not overlap.  rows and cols must be multiples of 8 and
+ * param, grad and momentum 16-byte aligned (else MUON_ERR_UNSUPPORTED).
+ * Errors: MUON_ERR_INVALID_ARG as the three calls; MUON_ERR_NO_MEMORY for a
+ * workspace smaller than required or a failed allocation.
+ */
+size_t muon_step_workspace_bytes(int64_t batch, int64_t rows, int64_t cols);
+int muon_step_batched(void *param, const void *grad, float *momentum, int64_t batch, int64_t rows, int64_t cols,
+                      float mu, int nesterov, int steps, const float coeffs[3], float eps, float lr,
+                      float weight_decay, float scale, void *workspace, size_t workspace_bytes,
+                      muon_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * The whole Muon step on matrices that live in host memory (FlexShard
  * section: with the parameters offloaded to host memory, Newton-Schulz runs on
  * the GPU).  param_host (bf16, in/out), grad_host (bf16) and momentum_host

@@ -60,6 +60,8 @@ SIGNATURES = {
     "muon_apply_update": (_INT, [_P, _P, _I64, _I64, _I64, _F, _F, _F, _P]),
     "muon_apply_update_f32": (_INT, [_P, _P, _I64, _I64, _I64, _F, _F, _F, _P]),
     "muon_default_scale": (_F, [_I64, _I64]),
+    "muon_step_workspace_bytes": (_SIZE, [_I64, _I64, _I64]),
+    "muon_step_batched": (_INT, [_P, _P, _P, _I64, _I64, _I64, _F, _INT, _INT, _P, _F, _F, _F, _F, _P, _SIZE, _P]),
     "muon_step_host": (_INT, [_P, _P, _P, _I64, _I64, _I64, _F, _INT, _INT, _P, _F, _F, _F, _F, _I64, _P]),
     "muon_adamw_update": (_INT, [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P]),
     "muon_adamw_update_f32": (_INT, [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P]),
@@ -299,6 +301,37 @@ def muon_adamw_update_f32(param, grad, exp_avg, exp_avg_sq, step, lr=1e-3, beta1
         float(beta2), float(eps), float(weight_decay), int(step), _stream_handle(stream)))
 
 
+def muon_step_workspace_bytes(batch, rows, cols):
+    return int(lib().muon_step_workspace_bytes(batch, rows, cols))
+
+
+def muon_step_batched(param, grad, momentum, *, mu=0.95, nesterov=True, steps=5, coeffs=QUINTIC, eps=1e-7, lr=0.02,
+                      weight_decay=0.1, scale=0.0, workspace=None, stream=None):
+    """The fused Muon step on one group of same-shape device matrices (in place).
+
+    param and grad bf16 (batch, rows, cols), momentum fp32 of the same shape.
+    Bit for bit the result of momentum -> Newton-Schulz -> update.  With
+    ``workspace`` (CUDA uint8, at least ``muon_step_workspace_bytes``) no
+    device memory is allocated; without it the library allocates it
+    stream-ordered.
+    """
+    import torch
+    _need(param, torch.bfloat16, "param")
+    _need(grad, torch.bfloat16, "grad")
+    _need(momentum, torch.float32, "momentum")
+    if not (param.shape == grad.shape == momentum.shape):
+        raise ValueError("param, grad and momentum must have the same shape")
+    b, r, c = _bmn(param)
+    ws, ws_bytes = None, 0
+    if workspace is not None:
+        _need(workspace, torch.uint8, "workspace")
+        ws, ws_bytes = _ptr(workspace), workspace.numel()
+    _check("muon_step_batched", lib().muon_step_batched(
+        _ptr(param), _ptr(grad), _ptr(momentum), b, r, c, float(mu), int(bool(nesterov)), int(steps),
+        _coeffs(coeffs), float(eps), float(lr), float(weight_decay), float(scale), ws, ws_bytes,
+        _stream_handle(stream)))
+
+
 def muon_step_host(param_host, grad_host, momentum_host, *, mu=0.95, nesterov=True, steps=5, coeffs=QUINTIC,
                    eps=1e-7, lr=0.02, weight_decay=0.1, scale=0.0, chunk=0, stream=None):
     """One Muon step on pinned host tensors (batch, rows, cols), streamed through the GPU."""
@@ -356,15 +389,24 @@ def muon_trace_end():
 
 
 # ---------------------------------------------------------------------------- one whole step
-def muon_step(params, grads, momenta, update_bufs, *, mu=0.95, nesterov=True, steps=5, coeffs=QUINTIC, eps=1e-7,
-              lr=0.02, weight_decay=0.1, scale=0.0, stream=None):
+def muon_step(params, grads, momenta, update_bufs=None, *, mu=0.95, nesterov=True, steps=5, coeffs=QUINTIC,
+              eps=1e-7, lr=0.02, weight_decay=0.1, scale=0.0, workspace=None, stream=None):
     """One Muon step over groups of same-shape matrices.
 
     Each argument is a list of tensors, one per shape group: params and grads
-    bf16 (batch, rows, cols), momenta fp32 of the same shape, update_bufs bf16
-    scratch of the same shape (receives u, then the orthogonalised update).
-    Per group: momentum -> batched Newton-Schulz -> update.
+    bf16 (batch, rows, cols), momenta fp32 of the same shape.  Without
+    update_bufs each group runs the fused muon_step_batched (on ``workspace``,
+    one uint8 tensor large enough for the largest group, if given).  With
+    update_bufs (bf16 scratch of each group's shape) each group runs
+    momentum -> batched Newton-Schulz -> update as three calls, and the
+    buffers keep the orthogonalised update; the parameters and momenta come
+    out bit-identical either way.
     """
+    if update_bufs is None:
+        for p, g, m in zip(params, grads, momenta):
+            muon_step_batched(p, g, m, mu=mu, nesterov=nesterov, steps=steps, coeffs=coeffs, eps=eps, lr=lr,
+                              weight_decay=weight_decay, scale=scale, workspace=workspace, stream=stream)
+        return
     for p, g, m, u in zip(params, grads, momenta, update_bufs):
         muon_momentum_update(g, m, u, mu, nesterov, stream)
         muon_ns_batched(u, steps, coeffs, eps, stream)

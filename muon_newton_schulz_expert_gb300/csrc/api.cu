@@ -32,7 +32,8 @@ std::atomic<int64_t> g_launches{0};
 const char *kTraceNames[kTraceKinds] = {"momentum_bf16", "momentum_f32", "norm_partial", "norm_final",
                                         "transpose",     "scale",        "ns_syrk_tc",   "ns_poly_tc",
                                         "ns_axpy_tc",    "apply_bf16",   "apply_f32",    "gemm_f32",
-                                        "copy",          "selftest_wait", "adamw"};
+                                        "copy",          "selftest_wait", "adamw",       "momentum_norm_bf16",
+                                        "ns_axpy_apply_tc"};
 
 struct TraceRec {
   int kind;
@@ -420,6 +421,73 @@ int muon_apply_update_f32(float *param, const float *update, int64_t batch, int6
   float kw, ko;
   update_constants(rows, cols, lr, weight_decay, scale, &kw, &ko);
   return launch_apply_f32(param, update, numel, kw, ko, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t muon_step_workspace_bytes(int64_t batch, int64_t rows, int64_t cols) {
+  return muon_ns_workspace_bytes(batch, rows, cols);
+}
+
+// momentum+norm -> iterations 1..steps-1 -> last iteration with the update.
+// u lives in the second X buffer, which the rotation first writes in
+// iteration 2, after iteration 1 has read u for the last time.
+static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, const Workspace &w, int64_t batch,
+                      int64_t rows, int64_t cols, float mu, int nesterov, int steps, const float *cf, float eps,
+                      float kw, float ko, cudaStream_t s) {
+  const int64_t mm = std::min(rows, cols), nn = std::max(rows, cols), per = rows * cols;
+  const bool transposed = rows > cols;
+  auto *x1 = static_cast<__nv_bfloat16 *>(w.x1);
+  auto *x2 = static_cast<__nv_bfloat16 *>(w.x2);
+  auto *A = static_cast<__nv_bfloat16 *>(w.a);
+  auto *B = static_cast<__nv_bfloat16 *>(w.b);
+  auto *lo = static_cast<__nv_bfloat16 *>(w.lo);
+  MUON_TRY(launch_momentum_norm_bf16(G, mom, x2, batch, per, mu, nesterov, eps, w.partial, w.inv, w.inv2, s));
+  if (steps == 0) {
+    MUON_TRY(launch_scale_bf16(x2, x2, batch, per, w.inv, s));
+    return launch_apply_bf16(W, x2, batch * per, kw, ko, s);
+  }
+  __nv_bfloat16 *src = x2;
+  for (int it = 0; it < steps; ++it) {
+    MUON_TRY(ns_syrk(src, A, batch, mm, nn, it == 0 ? w.inv2 : nullptr, transposed, s));
+    MUON_TRY(ns_poly(A, B, batch, mm, cf[1], cf[2], s));
+    const __nv_bfloat16 *src_lo = it == 0 ? nullptr : lo;
+    const float *s1 = it == 0 ? w.inv : nullptr;
+    if (it == steps - 1)
+      return ns_axpy_apply(B, src, src_lo, W, batch, mm, nn, cf[0], s1, kw, ko, transposed, s);
+    __nv_bfloat16 *dst = src == x1 ? x2 : x1;
+    MUON_TRY(ns_axpy(B, src, src_lo, dst, lo, batch, mm, nn, cf[0], s1, transposed, s));
+    src = dst;
+  }
+  return MUON_OK;
+}
+
+int muon_step_batched(void *param, const void *grad, float *momentum, int64_t batch, int64_t rows, int64_t cols,
+                      float mu, int nesterov, int steps, const float coeffs[3], float eps, float lr,
+                      float weight_decay, float scale, void *workspace, size_t workspace_bytes,
+                      muon_stream_t stream) {
+  MUON_TRY(check_ns_args(param, batch, rows, cols, steps, coeffs, eps));
+  if (!isfinite(mu) || !isfinite(lr) || !isfinite(weight_decay) || !isfinite(scale)) return MUON_ERR_INVALID_ARG;
+  if (batch == 0) return MUON_OK;
+  if (!grad || !momentum) return MUON_ERR_INVALID_ARG;
+  if (rows % 8 || cols % 8 || !aligned16(param) || !aligned16(grad) || !aligned16(momentum))
+    return MUON_ERR_UNSUPPORTED;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MUON_ERR_INVALID_ARG;
+  const int64_t mm = std::min(rows, cols), nn = std::max(rows, cols);
+  const size_t need = ws_bytes(batch, mm, nn, 2);
+  if (workspace && workspace_bytes < need) return MUON_ERR_NO_MEMORY;
+  if (!device_error_word()) return MUON_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float kw, ko;
+  update_constants(rows, cols, lr, weight_decay, scale, &kw, &ko);
+  const float cf[3] = {coeffs[0], coeffs[1], coeffs[2]};
+  void *ws = workspace;
+  if (!ws && (cudaMallocAsync(&ws, need, s) != cudaSuccess || !ws)) {
+    cudaGetLastError();
+    return MUON_ERR_NO_MEMORY;
+  }
+  int st = step_fused(static_cast<__nv_bfloat16 *>(param), static_cast<const __nv_bfloat16 *>(grad), momentum,
+                      carve(ws, batch, mm, nn, 2), batch, rows, cols, mu, nesterov ? 1 : 0, steps, cf, eps, kw, ko, s);
+  if (!workspace && cudaFreeAsync(ws, s) != cudaSuccess && st == MUON_OK) st = MUON_ERR_CUDA;
+  return st;
 }
 
 static int adamw_consts(float lr, float beta1, float beta2, float eps, float wd, int64_t step, AdamWConsts *k) {

@@ -30,6 +30,8 @@ enum TraceKind : int {
   kTraceCopy,
   kTraceSelftest,
   kTraceAdamW,
+  kTraceMomentumNorm,  // momentum fused with the per-matrix sum of squares
+  kTraceAxpyApply,     // last iteration's X' = s (a X + B X) fused with W' = kw W + ko X'
   kTraceKinds
 };
 
@@ -63,6 +65,12 @@ int launch_adamw_f32(float *w, const float *g, float *m, float *v, int64_t numel
 int norm_partials();
 int launch_inv_norm_bf16(const __nv_bfloat16 *x, int64_t batch, int64_t per, float eps, float *partial,
                          float *inv, float *inv2, cudaStream_t s);
+// Momentum (as launch_momentum_bf16) on [batch][per] matrices, fused with the
+// per-matrix inverse norm of the bf16 update u (as launch_inv_norm_bf16, with
+// the same partial sums).  Requires per % 8 == 0 and 16-byte aligned arrays.
+int launch_momentum_norm_bf16(const __nv_bfloat16 *g, float *buf, __nv_bfloat16 *u, int64_t batch, int64_t per,
+                              float mu, int nesterov, float eps, float *partial, float *inv, float *inv2,
+                              cudaStream_t s);
 int launch_inv_norm_f32(const float *x, int64_t batch, int64_t per, float eps, float *partial, float *inv,
                         float *inv2, cudaStream_t s);
 // dst[b] = src[b]^T for [batch][rows][cols] -> [batch][cols][rows]
@@ -92,6 +100,12 @@ int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, 
 int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *Xn,
             __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, bool transposed,
             cudaStream_t s);
+// The last iteration with the parameter update fused in: O = bf16(s1[b] *
+// (a*X + B X)) is not stored; W = bf16(kw*W + ko*O) in place, with W stored
+// in the same orientation as X.
+int ns_axpy_apply(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *W,
+                  int64_t batch, int64_t m, int64_t n, float a, const float *s1, float kw, float ko, bool transposed,
+                  cudaStream_t s);
 int selftest_wait(unsigned long long timeout_ns, cudaStream_t s);
 
 // ---- fp32 SIMT GEMMs for the verification mode (gemm_f32.cu) ----

@@ -247,6 +247,43 @@ __global__ void sumsq_bf16(const __nv_bfloat16 *__restrict__ x, int64_t per, flo
   if (threadIdx.x == 0) partial[b * kNormPartials + blockIdx.x] = s;
 }
 
+// Momentum on one chunk of one matrix, fused with the sum of squares of the
+// bf16 update it writes.  Block (j, b) covers exactly the elements and visits
+// them in exactly the order of sumsq_bf16<true>'s block (j, b), so the partial
+// sums, and hence the norms, equal those of momentum followed by the norm.
+__global__ void momentum_sumsq_bf16(const uint4 *__restrict__ g8, float4 *__restrict__ buf4, uint4 *__restrict__ u8,
+                                    int64_t per, float mu, int nesterov, float *__restrict__ partial) {
+  const int64_t b = blockIdx.y;
+  const int64_t chunk = (per + kNormPartials - 1) / kNormPartials;
+  const int64_t lo = ((int64_t)blockIdx.x * chunk + 7) & ~int64_t(7);
+  const int64_t hi =
+      blockIdx.x == kNormPartials - 1 ? per : min(per, ((int64_t)(blockIdx.x + 1) * chunk + 7) & ~int64_t(7));
+  const int64_t base = b * (per / 8);
+  float acc0 = 0.f, acc1 = 0.f;
+  for (int64_t i = base + lo / 8 + threadIdx.x; i < base + hi / 8; i += kThreads) {
+    Bf16x8 g;
+    g.v = __ldcs(g8 + i);
+    float4 b0 = __ldcs(buf4 + 2 * i), b1 = __ldcs(buf4 + 2 * i + 1);
+    float bf[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    Bf16x8 u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 gf = __bfloat1622float2(g.h[k]);
+      bf[2 * k] = mom_buf(mu, bf[2 * k], gf.x);
+      bf[2 * k + 1] = mom_buf(mu, bf[2 * k + 1], gf.y);
+      u.h[k] = __floats2bfloat162_rn(mom_u(mu, bf[2 * k], gf.x, nesterov), mom_u(mu, bf[2 * k + 1], gf.y, nesterov));
+      const float2 f = __bfloat1622float2(u.h[k]);
+      acc0 = fmaf(f.x, f.x, acc0);
+      acc1 = fmaf(f.y, f.y, acc1);
+    }
+    __stcs(buf4 + 2 * i, make_float4(bf[0], bf[1], bf[2], bf[3]));
+    __stcs(buf4 + 2 * i + 1, make_float4(bf[4], bf[5], bf[6], bf[7]));
+    u8[i] = u.v;  // read next by the first Newton-Schulz iteration: normal caching
+  }
+  float t = block_sum(acc0 + acc1);
+  if (threadIdx.x == 0) partial[b * kNormPartials + blockIdx.x] = t;
+}
+
 __global__ void sumsq_f32(const float *__restrict__ x, int64_t per, float *__restrict__ partial) {
   const int64_t b = blockIdx.y;
   const float *xb = x + b * per;
@@ -445,6 +482,24 @@ int launch_inv_norm_bf16(const __nv_bfloat16 *x, int64_t batch, int64_t per, flo
     else
       sumsq_bf16<false><<<grid, kThreads, 0, s>>>(x + b0 * per, per, partial + b0 * kNormPartials);
     int st = trace_after(kTraceNormPartial, s);
+    if (st) return st;
+  }
+  return launch_final(partial, batch, eps, inv, inv2, s);
+}
+
+int launch_momentum_norm_bf16(const __nv_bfloat16 *g, float *buf, __nv_bfloat16 *u, int64_t batch, int64_t per,
+                              float mu, int nesterov, float eps, float *partial, float *inv, float *inv2,
+                              cudaStream_t s) {
+  if (per % 8 || !aligned16(g) || !aligned16(buf) || !aligned16(u)) return MUON_ERR_UNSUPPORTED;
+  for (int64_t b0 = 0; b0 < batch; b0 += kMaxGridY) {
+    int64_t nb = std::min(kMaxGridY, batch - b0);
+    dim3 grid(kNormPartials, (unsigned)nb);
+    trace_before(kTraceMomentumNorm, s);
+    momentum_sumsq_bf16<<<grid, kThreads, 0, s>>>(reinterpret_cast<const uint4 *>(g + b0 * per),
+                                                  reinterpret_cast<float4 *>(buf + b0 * per),
+                                                  reinterpret_cast<uint4 *>(u + b0 * per), per, mu, nesterov,
+                                                  partial + b0 * kNormPartials);
+    int st = trace_after(kTraceMomentumNorm, s);
     if (st) return st;
   }
   return launch_final(partial, batch, eps, inv, inv2, s);

@@ -77,6 +77,12 @@ constexpr int UMMA_K = 16;
 #ifndef MUON_SLOTS_AXPY
 #define MUON_SLOTS_AXPY 2
 #endif
+#ifndef MUON_STAGES_APPLY
+#define MUON_STAGES_APPLY 4
+#endif
+#ifndef MUON_SLOTS_APPLY
+#define MUON_SLOTS_APPLY 1
+#endif
 constexpr int A_STAGE = BM * BK * 2;   // 16 KB
 constexpr int B_STAGE = BNH * BK * 2;  // 16 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
@@ -91,17 +97,30 @@ constexpr int ACC_COLS = BN;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int CHUNKS = BN / 2 / 32;  // 32-column chunks per epilogue thread and tile
 
-enum Epi { EPI_SYRK = 0, EPI_POLY = 1, EPI_AXPY = 2 };
+// EPI_APPLY is the last iteration's AXPY with the parameter update fused in:
+// it reads the parameter W instead of writing X's halves, and writes
+// W' = kw W + ko bf16(X') in place.
+enum Epi { EPI_SYRK = 0, EPI_POLY = 1, EPI_AXPY = 2, EPI_APPLY = 3 };
 
 template <int EPI>
 struct Layout {
-  static constexpr int stages =
-      EPI == EPI_AXPY ? MUON_STAGES_AXPY : (EPI == EPI_POLY ? MUON_STAGES_POLY : MUON_STAGES_SYRK);
-  static constexpr int slots = EPI == EPI_AXPY ? MUON_SLOTS_AXPY : (EPI == EPI_POLY ? MUON_SLOTS_POLY : MUON_SLOTS_SYRK);
-  // AXPY stages its output in a box of its own, so that fetching the next
-  // input never waits for the previous store to finish reading.
-  static constexpr int out_slots = EPI == EPI_AXPY ? 1 : 0;
-  static constexpr int epi_bytes = EPI_WARPS * (slots + out_slots) * EPI_BUF;
+  static constexpr int stages = EPI == EPI_APPLY  ? MUON_STAGES_APPLY
+                                : EPI == EPI_AXPY ? MUON_STAGES_AXPY
+                                : EPI == EPI_POLY ? MUON_STAGES_POLY
+                                                  : MUON_STAGES_SYRK;
+  static constexpr int slots = EPI == EPI_APPLY  ? MUON_SLOTS_APPLY
+                               : EPI == EPI_AXPY ? MUON_SLOTS_AXPY
+                               : EPI == EPI_POLY ? MUON_SLOTS_POLY
+                                                 : MUON_SLOTS_SYRK;
+  // Bytes of one input slot and of the output slot per epilogue warp.
+  // SYRK/POLY: a slot is [direct box][mirror box], with no separate output.
+  // AXPY: input [X hi][X lo], output [X' hi][X' lo]; APPLY: input
+  // [X hi][X lo][W], output [W'].  The output has a box of its own, so that
+  // fetching the next input never waits for the previous store to finish
+  // reading.
+  static constexpr int in_bytes = (EPI == EPI_APPLY ? 3 : 2) * EPI_BOX_BYTES;
+  static constexpr int out_bytes = EPI == EPI_APPLY ? EPI_BOX_BYTES : EPI == EPI_AXPY ? 2 * EPI_BOX_BYTES : 0;
+  static constexpr int epi_bytes = EPI_WARPS * (slots * in_bytes + out_bytes);
   static constexpr int num_bars = 2 * stages + 5 + EPI_WARPS * slots;
   static constexpr int smem_bytes = stages * STAGE_BYTES + epi_bytes + 1024 + num_bars * 8 + 16;
   static_assert(CHUNKS % slots == 0, "chunks per tile must fill the staging slots evenly");
@@ -127,6 +146,7 @@ struct Params {
   const __nv_bfloat16 *src_lo;
   __nv_bfloat16 *out_lo;
   float a, b, c;
+  float kw, ko;                // APPLY only: W' = kw W + ko O
   unsigned *err;
   unsigned long long timeout_ns;
 };
@@ -311,7 +331,7 @@ template <int EPI>
 __device__ __forceinline__ void decode_tile(const Params &p, long long t, int &mat, int &ti, int &tj) {
   mat = (int)(t / p.tiles_per_mat);
   int r = (int)(t - (long long)mat * p.tiles_per_mat);
-  if (EPI == EPI_AXPY) {
+  if (EPI >= EPI_AXPY) {
     tj = r / p.tiles_m;
     ti = r - tj * p.tiles_m;
   } else {
@@ -373,7 +393,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (EPI == EPI_AXPY) {
+    if (EPI >= EPI_AXPY) {
       tma_prefetch_desc(&p.tm_src);
       tma_prefetch_desc(&p.tm_out);
     }
@@ -486,32 +506,38 @@ __global__ void __launch_bounds__(THREADS, 1)
       volatile int no_abort = 0;
       wait_bounded(drain_bar, 0, Watch{&no_abort, p.err, p.timeout_ns});
     }
-  } else if (EPI == EPI_AXPY) {
+  } else if (EPI >= EPI_AXPY) {
     // ---------------------------------------------------------------- AXPY epilogue (both CTAs)
     // X' = s (a (hi + lo) + acc) through shared memory: each warp stages a
     // 32 x 32 box of hi and of lo (TMA load, zero-filled past the edges),
-    // overwrites it with hi' = bf16(X'), lo' = bf16(X' - hi') and TMA-stores
-    // it (clipped at the edges).  Lane i owns row i of the box, which is TMEM
-    // lane 32q + i; the 64-byte swizzle makes these row reads conflict-free.
-    // With two slots per warp the box of chunk g + 2 is fetched into the slot
-    // of chunk g as soon as g's store has read it, a whole chunk ahead of use.
+    // writes hi' = bf16(X'), lo' = bf16(X' - hi') to its output box and
+    // TMA-stores it (clipped at the edges).  APPLY also stages the box of W
+    // and stores W' = bf16(kw W + ko hi') in its place, the parameter update
+    // of the unfused path, operation for operation.  Lane i owns row i of the
+    // box, which is TMEM lane 32q + i; the 64-byte swizzle makes these row
+    // reads conflict-free.  With two slots per warp the box of chunk g + 2 is
+    // fetched into the slot of chunk g as soon as g has been computed, a whole
+    // chunk ahead of use.
+    constexpr bool APPLY = EPI == EPI_APPLY;
     constexpr int SLOTS = Layout<EPI>::slots;
+    constexpr int IN_BYTES = Layout<EPI>::in_bytes;
     const int ew = warp - 2;
     const int q = warp & 3, half = ew >> 2;
-    // SLOTS input slots of [hi box][lo box], then the output slot
-    uint8_t *ebase = epi_smem + ew * (SLOTS + 1) * EPI_BUF;
+    // SLOTS input slots, then the output slot
+    uint8_t *ebase = epi_smem + ew * (SLOTS * IN_BYTES + Layout<EPI>::out_bytes);
     const uint32_t ebase_s = smem_u32(ebase);
-    uint8_t *obuf = ebase + SLOTS * EPI_BUF;
-    const uint32_t obuf_s = ebase_s + SLOTS * EPI_BUF;
+    uint8_t *obuf = ebase + SLOTS * IN_BYTES;
+    const uint32_t obuf_s = ebase_s + SLOTS * IN_BYTES;
     uint32_t ephase_bits = 0;                                // parity per slot
-    const bool lo_in = p.src_lo != nullptr, lo_out = p.out_lo != nullptr;
-    const uint32_t etx = lo_in ? 2u * EPI_BOX_BYTES : (uint32_t)EPI_BOX_BYTES;
+    const bool lo_in = p.src_lo != nullptr, lo_out = !APPLY && p.out_lo != nullptr;
+    const uint32_t etx = (lo_in ? 2u : 1u) * EPI_BOX_BYTES + (APPLY ? (uint32_t)EPI_BOX_BYTES : 0u);
     auto epi_load = [&](int slot, int m_, int row0_, int col0_) {  // lane 0 only
-      const uint32_t dst = ebase_s + slot * EPI_BUF, bar = EBAR(ew * SLOTS + slot);
+      const uint32_t dst = ebase_s + slot * IN_BYTES, bar = EBAR(ew * SLOTS + slot);
       fence_proxy_async_smem();
       mbar_expect_tx(bar, etx);
       tma_load_3d(dst, &p.tm_src, bar, col0_, row0_, m_);
       if (lo_in) tma_load_3d(dst + EPI_BOX_BYTES, &p.tm_src_lo, bar, col0_, row0_, m_);
+      if (APPLY) tma_load_3d(dst + 2 * EPI_BOX_BYTES, &p.tm_out, bar, col0_, row0_, m_);  // W, stored over later
     };
     const int rbase = (int)rank * BM + q * 32;  // this warp's rows within a pair tile
     int acc = 0;
@@ -537,7 +563,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll 1
       for (int ch = 0; ch < CHUNKS; ++ch) {
         const int slot = ch % SLOTS;   // CHUNKS is a multiple of SLOTS
-        uint8_t *ebuf = ebase + slot * EPI_BUF;
+        uint8_t *ebuf = ebase + slot * IN_BYTES;
         const int col0 = tj * BN + half * 128 + ch * 32;
         const bool got = wait_bounded(EBAR(ew * SLOTS + slot), (ephase_bits >> slot) & 1u, w);
         if (!__all_sync(0xffffffffu, got)) {
@@ -553,9 +579,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint32_t off = (uint32_t)(lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
-          Pack8 hv, lv, ho, lo;
+          Pack8 hv, lv, wv, ho, lo;
           hv.v = *reinterpret_cast<const uint4 *>(ebuf + off);
           lv.v = lo_in ? *reinterpret_cast<const uint4 *>(ebuf + EPI_BOX_BYTES + off) : make_uint4(0u, 0u, 0u, 0u);
+          if (APPLY) wv.v = *reinterpret_cast<const uint4 *>(ebuf + 2 * EPI_BOX_BYTES + off);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int k = c * 8 + 2 * e;
@@ -564,7 +591,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float v1 = sc * fmaf(p.a, fh.y + fl.y, __uint_as_float(r[k + 1]));
             ho.h[e] = __floats2bfloat162_rn(v0, v1);
             const float2 hh = __bfloat1622float2(ho.h[e]);
-            lo.h[e] = __floats2bfloat162_rn(v0 - hh.x, v1 - hh.y);
+            if (APPLY) {  // W' = kw W + ko O, each product and the sum rounded separately
+              const float2 wf = __bfloat1622float2(wv.h[e]);
+              ho.h[e] = __floats2bfloat162_rn(__fadd_rn(__fmul_rn(p.kw, wf.x), __fmul_rn(p.ko, hh.x)),
+                                              __fadd_rn(__fmul_rn(p.kw, wf.y), __fmul_rn(p.ko, hh.y)));
+            } else {
+              lo.h[e] = __floats2bfloat162_rn(v0 - hh.x, v1 - hh.y);
+            }
           }
           *reinterpret_cast<uint4 *>(obuf + off) = ho.v;
           if (lo_out) *reinterpret_cast<uint4 *>(obuf + EPI_BOX_BYTES + off) = lo.v;
@@ -924,9 +957,14 @@ int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, 
   return launch<EPI_POLY, false, false>(ma, mb, p, kTracePoly, s);
 }
 
-int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *Xn,
-            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, bool transposed,
-            cudaStream_t s) {
+namespace {
+
+// X' = s1 (a X + B X) with X' written as Xn (+ Xn_lo), or, for EPI_APPLY,
+// folded into W' = kw W + ko bf16(X') with W in place of Xn.
+template <int EPI>
+int axpy_launch(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *Xn,
+                __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, float kw,
+                float ko, bool transposed, int trace_kind, cudaStream_t s) {
   CUtensorMap ma, mb;
   int st;
   Params p;
@@ -963,8 +1001,25 @@ int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 
   p.scale = s1;
   p.src_lo = X_lo;
   p.out_lo = Xn_lo;
-  return transposed ? launch<EPI_AXPY, false, false>(ma, mb, p, kTraceAxpy, s)
-                    : launch<EPI_AXPY, false, true>(ma, mb, p, kTraceAxpy, s);
+  p.kw = kw;
+  p.ko = ko;
+  return transposed ? launch<EPI, false, false>(ma, mb, p, trace_kind, s)
+                    : launch<EPI, false, true>(ma, mb, p, trace_kind, s);
+}
+
+}  // namespace
+
+int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *Xn,
+            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, bool transposed,
+            cudaStream_t s) {
+  return axpy_launch<EPI_AXPY>(B, X, X_lo, Xn, Xn_lo, batch, m, n, a, s1, 0.f, 0.f, transposed, kTraceAxpy, s);
+}
+
+int ns_axpy_apply(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *W,
+                  int64_t batch, int64_t m, int64_t n, float a, const float *s1, float kw, float ko, bool transposed,
+                  cudaStream_t s) {
+  return axpy_launch<EPI_APPLY>(B, X, X_lo, W, nullptr, batch, m, n, a, s1, kw, ko, transposed, kTraceAxpyApply,
+                                s);
 }
 
 int selftest_wait(unsigned long long timeout_ns, cudaStream_t s) {

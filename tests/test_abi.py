@@ -132,6 +132,26 @@ def test_newer_entry_points_reject_bad_arguments_on_the_host(lib):
     assert lib.muon_step_host(None, None, None, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, 0, None) == -1
     assert lib.muon_step_host(None, None, None, -1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, 0, None) == -1
     assert lib.muon_step_host(None, None, None, 1, 8, 8, 0.95, 1, 5, None, 1e-7, 0.02, 0.1, 0.0, 0, None) == -1
+    # fused device step: sizes, null pointers, shapes, alignment, workspace
+    P = ctypes.c_void_p(256)
+    assert lib.muon_step_batched(None, None, None, 0, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, None, 0, None) == 0
+    assert lib.muon_step_batched(None, P, P, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, None, 0, None) == -1
+    assert lib.muon_step_batched(P, None, P, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, None, 0, None) == -1
+    assert lib.muon_step_batched(P, P, None, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, None, 0, None) == -1
+    assert lib.muon_step_batched(P, P, P, 1, 12, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, None, 0, None) == -2
+    assert lib.muon_step_batched(ctypes.c_void_p(264), P, P, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0,
+                                 None, 0, None) == -2
+    assert lib.muon_step_batched(P, P, P, 1, 8, 8, 0.95, 1, 5, None, 1e-7, 0.02, 0.1, 0.0, None, 0, None) == -1
+    assert lib.muon_step_batched(P, P, P, 1, 8, 8, float("nan"), 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, None, 0,
+                                 None) == -1
+    assert lib.muon_step_batched(P, P, P, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, float("inf"), 0.1, 0.0, None, 0,
+                                 None) == -1
+    assert lib.muon_step_batched(P, P, P, 1, 8, 8, 0.95, 1, -1, c3, 1e-7, 0.02, 0.1, 0.0, None, 0, None) == -1
+    assert lib.muon_step_batched(P, P, P, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, ctypes.c_void_p(272),
+                                 1 << 20, None) == -1      # workspace not 256-byte aligned
+    assert lib.muon_step_batched(P, P, P, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, P, 64, None) == -4
+    assert lib.muon_step_workspace_bytes(96, 6144, 1792) == lib.muon_ns_workspace_bytes(96, 1792, 6144)
+    assert lib.muon_step_workspace_bytes(0, 8, 8) == 0
 
 
 def test_trace_without_gpu_work_is_empty(lib):
