@@ -56,9 +56,13 @@ constexpr int BNH = 128;   // rows of the B operand held by one CTA
 constexpr int BK = 64;     // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
 // Shared-memory split between the operand ring and the epilogue staging
-// slots (one slot = two 2 KB boxes per epilogue warp).  X X^T has a long K
-// loop and no epilogue operand: deeper ring, one slot.  The short-K kernels
-// stream an epilogue operand: two slots, so each box is fetched a chunk ahead.
+// slots (one slot = two or three 2 KB boxes per epilogue warp).  A stage is
+// complete only when its slowest sector has arrived, so the ring depth sets
+// how much L2/DRAM latency the tensor cores can ride out: each kernel gets as
+// many stages as fit beside its epilogue.  X X^T has a long K loop and no
+// epilogue operand: one slot.  bA + cAA streams b*A through two slots, so
+// each box is fetched a chunk ahead; aX + BX keeps one input slot and a
+// fifth stage, which measured faster than two slots and four stages.
 #ifndef MUON_STAGES_SYRK
 #define MUON_STAGES_SYRK 6
 #endif
@@ -72,10 +76,10 @@ constexpr int UMMA_K = 16;
 #define MUON_SLOTS_POLY 2
 #endif
 #ifndef MUON_STAGES_AXPY
-#define MUON_STAGES_AXPY 4
+#define MUON_STAGES_AXPY 5
 #endif
 #ifndef MUON_SLOTS_AXPY
-#define MUON_SLOTS_AXPY 2
+#define MUON_SLOTS_AXPY 1
 #endif
 #ifndef MUON_STAGES_APPLY
 #define MUON_STAGES_APPLY 4
@@ -515,9 +519,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     // and stores W' = bf16(kw W + ko hi') in its place, the parameter update
     // of the unfused path, operation for operation.  Lane i owns row i of the
     // box, which is TMEM lane 32q + i; the 64-byte swizzle makes these row
-    // reads conflict-free.  With two slots per warp the box of chunk g + 2 is
-    // fetched into the slot of chunk g as soon as g has been computed, a whole
-    // chunk ahead of use.
+    // reads conflict-free.  The boxes of chunk g + SLOTS are fetched into the
+    // slot of chunk g as soon as g has been computed (while g's result is
+    // being stored from the separate output box).
     constexpr bool APPLY = EPI == EPI_APPLY;
     constexpr int SLOTS = Layout<EPI>::slots;
     constexpr int IN_BYTES = Layout<EPI>::in_bytes;
