@@ -426,8 +426,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         decode_tile<EPI>(p, t, mat, ti, tj);
         const int arow = ti * CM + (int)rank * BM;    // this CTA's rows of A
         const int brow = tj * BN + (int)rank * BNH;   // this CTA's half of B
+        // aX + BX: tiles that share an operand block start their K loop at
+        // different offsets ((ti + tj) mod T of T segments), so that a
+        // block's first fetch from DRAM is waited on by one tile while the
+        // others read blocks already in L2.  The sum over K starts and wraps
+        // at the offset (a fixed order per tile).  The long-K symmetric
+        // kernels keep the plain order: there the rotation stretched the
+        // reuse distance past what L2 holds and measured slower.
+        const int kt = p.tiles_m > p.tiles_n ? p.tiles_m : p.tiles_n;
+        const int kb0 = EPI >= EPI_AXPY ? (int)((long long)((ti + tj) % kt) * num_kb / kt) : 0;
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int i = 0; i < num_kb; ++i) {
+          const int kb = kb0 + i < num_kb ? kb0 + i : kb0 + i - num_kb;
           if (!wait_bounded(EMPTY(stage), phase ^ 1u, w)) {
             ok = false;
             break;
@@ -475,7 +485,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * ACC_COLS);
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int i = 0; i < num_kb; ++i) {  // i-th k-block of the tile in the producer's order
           if (!wait_bounded(FULL(stage), phase, w)) {
             ok = false;
             break;
@@ -492,7 +502,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                         : smem_desc(sa + kk * (UMMA_K * 2), 16, 1024);
             const uint64_t bdesc = B_MN ? smem_desc(sb + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
                                         : smem_desc(sb + kk * (UMMA_K * 2), 16, 1024);
-            tc_mma(d, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma(d, adesc, bdesc, idesc, (i | kk) != 0 ? 1u : 0u);
           }
           tc_commit_mc(EMPTY(stage), 0x3);  // both CTAs may refill this stage
           if (++stage == STAGES) {
