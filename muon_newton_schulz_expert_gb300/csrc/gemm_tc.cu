@@ -26,7 +26,7 @@
 // shared memory, which is what keeps its bandwidth below the tensor cores'
 // appetite.
 //   warp 0 lane 0  TMA producer (both CTAs): 128x64 bf16 boxes, 128-byte
-//                  swizzle, a ring of 4-6 stages (Layout); completion is
+//                  swizzle, a ring of 5-6 stages (Layout); completion is
 //                  signalled on the even CTA's "full" barrier, which counts
 //                  the bytes of both halves;
 //   warp 1         TMEM allocation of 512 columns (two 128 x 256 fp32
@@ -61,8 +61,9 @@ constexpr int UMMA_K = 16;
 // how much L2/DRAM latency the tensor cores can ride out: each kernel gets as
 // many stages as fit beside its epilogue.  X X^T has a long K loop and no
 // epilogue operand: one slot.  bA + cAA streams b*A through two slots, so
-// each box is fetched a chunk ahead; aX + BX keeps one input slot and a
-// fifth stage, which measured faster than two slots and four stages.
+// each box is fetched a chunk ahead; aX + BX (also with the update) keeps one
+// input slot and a fifth stage, which measured faster than two slots and
+// four (three) stages.
 #ifndef MUON_STAGES_SYRK
 #define MUON_STAGES_SYRK 6
 #endif
@@ -82,7 +83,7 @@ constexpr int UMMA_K = 16;
 #define MUON_SLOTS_AXPY 1
 #endif
 #ifndef MUON_STAGES_APPLY
-#define MUON_STAGES_APPLY 4
+#define MUON_STAGES_APPLY 5
 #endif
 #ifndef MUON_SLOTS_APPLY
 #define MUON_SLOTS_APPLY 1
