@@ -26,7 +26,8 @@
 // shared memory, which is what keeps its bandwidth below the tensor cores'
 // appetite.
 //   warp 0 lane 0  TMA producer (both CTAs): 128x64 bf16 boxes, 128-byte
-//                  swizzle, a ring of 5-6 stages (Layout); completion is
+//                  swizzle, a ring of 3 two-k-block or 5 one-k-block
+//                  stages (Layout); completion is
 //                  signalled on the even CTA's "full" barrier, which counts
 //                  the bytes of both halves;
 //   warp 1         TMEM allocation of 512 columns (two 128 x 256 fp32
@@ -55,29 +56,48 @@ constexpr int BN = 256;    // columns of a pair tile
 constexpr int BNH = 128;   // rows of the B operand held by one CTA
 constexpr int BK = 64;     // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
-// Shared-memory split between the operand ring and the epilogue staging
-// slots (one slot = two or three 2 KB boxes per epilogue warp).  A stage is
-// complete only when its slowest sector has arrived, so the ring depth sets
-// how much L2/DRAM latency the tensor cores can ride out: each kernel gets as
-// many stages as fit beside its epilogue.  X X^T has a long K loop and no
-// epilogue operand: one slot.  bA + cAA streams b*A through two slots, so
-// each box is fetched a chunk ahead; aX + BX (also with the update) keeps one
-// input slot and a fifth stage, which measured faster than two slots and
-// four (three) stages.
+// Operand ring and epilogue staging share the CTA's shared memory.
+//  - A stage holds KSUB k-blocks of 64 (32 KB per k-block: 128 rows of A and
+//    a 128-row half of B) behind one full/empty barrier pair.  Each handoff
+//    (MMA commit -> producer refill -> TMA completion -> MMA issue) has a
+//    fixed cost, so two k-blocks per stage (8 MMAs per handoff) run the
+//    mainloop 4-9% faster than one where three such stages fit.
+//  - A stage completes only when its slowest sector arrives, so the ring must
+//    hold ~160-192 KB in flight to ride out L2/DRAM latency.
+//  - Epilogue slots: one slot = two or three 2 KB boxes per epilogue warp.
+//    X X^T: one slot (output staging).  bA + cAA: one slot (b*A in, result
+//    over it).  aX + BX: one slot of X's halves, the result written over it,
+//    so 3 double stages fit.  aX + BX with the update: three input boxes and
+//    a separate output box, which leaves room for 5 single stages.
+#ifndef MUON_AXPY_INPLACE
+#define MUON_AXPY_INPLACE 1
+#endif
+#ifndef MUON_KSUB_SYRK
+#define MUON_KSUB_SYRK 2
+#endif
+#ifndef MUON_KSUB_POLY
+#define MUON_KSUB_POLY 2
+#endif
+#ifndef MUON_KSUB_AXPY
+#define MUON_KSUB_AXPY 2
+#endif
+#ifndef MUON_KSUB_APPLY
+#define MUON_KSUB_APPLY 1
+#endif
 #ifndef MUON_STAGES_SYRK
-#define MUON_STAGES_SYRK 6
+#define MUON_STAGES_SYRK 3
 #endif
 #ifndef MUON_SLOTS_SYRK
 #define MUON_SLOTS_SYRK 1
 #endif
 #ifndef MUON_STAGES_POLY
-#define MUON_STAGES_POLY 5
+#define MUON_STAGES_POLY 3
 #endif
 #ifndef MUON_SLOTS_POLY
-#define MUON_SLOTS_POLY 2
+#define MUON_SLOTS_POLY 1
 #endif
 #ifndef MUON_STAGES_AXPY
-#define MUON_STAGES_AXPY 5
+#define MUON_STAGES_AXPY 3
 #endif
 #ifndef MUON_SLOTS_AXPY
 #define MUON_SLOTS_AXPY 1
@@ -119,15 +139,23 @@ struct Layout {
                                                  : MUON_SLOTS_SYRK;
   // Bytes of one input slot and of the output slot per epilogue warp.
   // SYRK/POLY: a slot is [direct box][mirror box], with no separate output.
-  // AXPY: input [X hi][X lo], output [X' hi][X' lo]; APPLY: input
-  // [X hi][X lo][W], output [W'].  The output has a box of its own, so that
-  // fetching the next input never waits for the previous store to finish
-  // reading.
+  // AXPY: input [X hi][X lo], the result [X' hi][X' lo] written over it (or,
+  // with MUON_AXPY_INPLACE 0, into an output box of its own); APPLY: input
+  // [X hi][X lo][W], output [W'] in a box of its own, so that fetching the
+  // next input never waits for the previous store to finish reading.
   static constexpr int in_bytes = (EPI == EPI_APPLY ? 3 : 2) * EPI_BOX_BYTES;
-  static constexpr int out_bytes = EPI == EPI_APPLY ? EPI_BOX_BYTES : EPI == EPI_AXPY ? 2 * EPI_BOX_BYTES : 0;
+  static constexpr bool inplace = EPI == EPI_AXPY && MUON_AXPY_INPLACE != 0;
+  static constexpr int out_bytes =
+      EPI == EPI_APPLY ? EPI_BOX_BYTES : (EPI == EPI_AXPY && !inplace) ? 2 * EPI_BOX_BYTES : 0;
   static constexpr int epi_bytes = EPI_WARPS * (slots * in_bytes + out_bytes);
   static constexpr int num_bars = 2 * stages + 5 + EPI_WARPS * slots;
-  static constexpr int smem_bytes = stages * STAGE_BYTES + epi_bytes + 1024 + num_bars * 8 + 16;
+  // k-blocks of 64 per stage (one barrier round trip per ksub k-blocks)
+  static constexpr int ksub = EPI == EPI_APPLY  ? MUON_KSUB_APPLY
+                              : EPI == EPI_AXPY ? MUON_KSUB_AXPY
+                              : EPI == EPI_POLY ? MUON_KSUB_POLY
+                                                : MUON_KSUB_SYRK;
+  static constexpr int stage_bytes = ksub * STAGE_BYTES;
+  static constexpr int smem_bytes = stages * stage_bytes + epi_bytes + 1024 + num_bars * 8 + 16;
   static_assert(CHUNKS % slots == 0, "chunks per tile must fill the staging slots evenly");
   static_assert(smem_bytes <= 232448, "shared memory per CTA");
 };
@@ -364,7 +392,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int STAGES = Layout<EPI>::stages;
-  uint8_t *epi_smem = smem + STAGES * STAGE_BYTES;  // AXPY staging slots, 1024-aligned
+  constexpr int KSUB = Layout<EPI>::ksub;
+  constexpr int SBYTES = Layout<EPI>::stage_bytes;
+  uint8_t *epi_smem = smem + STAGES * SBYTES;  // AXPY staging slots, 1024-aligned
   uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + Layout<EPI>::epi_bytes);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Layout<EPI>::num_bars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -416,6 +446,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const Watch w{abort_flag, p.err, p.timeout_ns};
   const int num_kb = (p.K + BK - 1) / BK;
+  const int num_steps = (num_kb + KSUB - 1) / KSUB;  // stages per tile
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer (both CTAs)
@@ -437,33 +468,39 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int kt = p.tiles_m > p.tiles_n ? p.tiles_m : p.tiles_n;
         const int kb0 = EPI >= EPI_AXPY ? (int)((long long)((ti + tj) % kt) * num_kb / kt) : 0;
         bool ok = true;
-        for (int i = 0; i < num_kb; ++i) {
-          const int kb = kb0 + i < num_kb ? kb0 + i : kb0 + i - num_kb;
+        for (int i = 0; i < num_steps; ++i) {
           if (!wait_bounded(EMPTY(stage), phase ^ 1u, w)) {
             ok = false;
             break;
           }
+          const int valid = num_kb - i * KSUB < KSUB ? num_kb - i * KSUB : KSUB;
           // CTA 0's barrier counts the bytes of both halves; CTA 1's loads only
           // complete bytes on it (a stage is refilled only after the MMAs that
           // read it finished, so no load can run ahead into the next phase)
           const uint32_t full0 = map_to_rank(FULL(stage), 0);
-          if (rank == 0) mbar_expect_tx(FULL(stage), 2 * STAGE_BYTES);
-          const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_STAGE;
-          // K-major operands: one box of 128 rows x 64 K-columns.  MN-major
-          // operands: boxes of 64 M/N-columns x 64 K-rows, one per swizzle atom.
-          if (!A_MN) {
-            tma_load_3d_pair(sa, &tmA, full0, kb * BK, arow, mat);
-          } else {
+          if (rank == 0) mbar_expect_tx(FULL(stage), 2 * valid * STAGE_BYTES);
 #pragma unroll
-            for (int q = 0; q < BM / 64; ++q)
-              tma_load_3d_pair(sa + q * (64 * BK * 2), &tmA, full0, arow + q * 64, kb * BK, mat);
-          }
-          if (!B_MN) {
-            tma_load_3d_pair(sb, &tmB, full0, kb * BK, brow, mat);
-          } else {
+          for (int j = 0; j < KSUB; ++j) {
+            if (j >= valid) break;
+            const int ki = i * KSUB + j;
+            const int kb = kb0 + ki < num_kb ? kb0 + ki : kb0 + ki - num_kb;
+            const uint32_t sa = sbase + stage * SBYTES + j * STAGE_BYTES, sb = sa + A_STAGE;
+            // K-major operands: one box of 128 rows x 64 K-columns.  MN-major
+            // operands: boxes of 64 M/N-columns x 64 K-rows, one per swizzle atom.
+            if (!A_MN) {
+              tma_load_3d_pair(sa, &tmA, full0, kb * BK, arow, mat);
+            } else {
 #pragma unroll
-            for (int q = 0; q < BNH / 64; ++q)
-              tma_load_3d_pair(sb + q * (64 * BK * 2), &tmB, full0, brow + q * 64, kb * BK, mat);
+              for (int q = 0; q < BM / 64; ++q)
+                tma_load_3d_pair(sa + q * (64 * BK * 2), &tmA, full0, arow + q * 64, kb * BK, mat);
+            }
+            if (!B_MN) {
+              tma_load_3d_pair(sb, &tmB, full0, kb * BK, brow, mat);
+            } else {
+#pragma unroll
+              for (int q = 0; q < BNH / 64; ++q)
+                tma_load_3d_pair(sb + q * (64 * BK * 2), &tmB, full0, brow + q * 64, kb * BK, mat);
+            }
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -486,24 +523,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * ACC_COLS);
         bool ok = true;
-        for (int i = 0; i < num_kb; ++i) {  // i-th k-block of the tile in the producer's order
+        for (int i = 0; i < num_steps; ++i) {  // i-th stage of the tile in the producer's order
           if (!wait_bounded(FULL(stage), phase, w)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_STAGE;
+          const int valid = num_kb - i * KSUB < KSUB ? num_kb - i * KSUB : KSUB;
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            // K-major: advance 16 K-elements (32 bytes) inside the swizzle row.
-            // MN-major: advance 16 K-rows (two 8-row groups of 1024 bytes);
-            // LBO = 8192 bytes between 64-wide atoms, SBO = 1024 between K groups.
-            // The same shared-memory offsets address the peer CTA's halves.
-            const uint64_t adesc = A_MN ? smem_desc(sa + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
-                                        : smem_desc(sa + kk * (UMMA_K * 2), 16, 1024);
-            const uint64_t bdesc = B_MN ? smem_desc(sb + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
-                                        : smem_desc(sb + kk * (UMMA_K * 2), 16, 1024);
-            tc_mma(d, adesc, bdesc, idesc, (i | kk) != 0 ? 1u : 0u);
+          for (int j = 0; j < KSUB; ++j) {
+            if (j >= valid) break;
+            const uint32_t sa = sbase + stage * SBYTES + j * STAGE_BYTES, sb = sa + A_STAGE;
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              // K-major: advance 16 K-elements (32 bytes) inside the swizzle row.
+              // MN-major: advance 16 K-rows (two 8-row groups of 1024 bytes);
+              // LBO = 8192 bytes between 64-wide atoms, SBO = 1024 between K groups.
+              // The same shared-memory offsets address the peer CTA's halves.
+              const uint64_t adesc = A_MN ? smem_desc(sa + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
+                                          : smem_desc(sa + kk * (UMMA_K * 2), 16, 1024);
+              const uint64_t bdesc = B_MN ? smem_desc(sb + kk * (UMMA_K * 128), 64 * BK * 2, 1024)
+                                          : smem_desc(sb + kk * (UMMA_K * 2), 16, 1024);
+              tc_mma(d, adesc, bdesc, idesc, ((i * KSUB + j) | kk) != 0 ? 1u : 0u);
+            }
           }
           tc_commit_mc(EMPTY(stage), 0x3);  // both CTAs may refill this stage
           if (++stage == STAGES) {
@@ -525,15 +567,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------------------------------------------------------- AXPY epilogue (both CTAs)
     // X' = s (a (hi + lo) + acc) through shared memory: each warp stages a
     // 32 x 32 box of hi and of lo (TMA load, zero-filled past the edges),
-    // writes hi' = bf16(X'), lo' = bf16(X' - hi') to its output box and
-    // TMA-stores it (clipped at the edges).  APPLY also stages the box of W
-    // and stores W' = bf16(kw W + ko hi') in its place, the parameter update
-    // of the unfused path, operation for operation.  Lane i owns row i of the
-    // box, which is TMEM lane 32q + i; the 64-byte swizzle makes these row
-    // reads conflict-free.  The boxes of chunk g + SLOTS are fetched into the
-    // slot of chunk g as soon as g has been computed (while g's result is
-    // being stored from the separate output box).
+    // writes hi' = bf16(X'), lo' = bf16(X' - hi') over it (each lane over
+    // what it has just read) and TMA-stores it (clipped at the edges); the
+    // boxes of chunk g + SLOTS are fetched into the slot once that store has
+    // read it.  APPLY also stages the box of W and writes W' = bf16(kw W +
+    // ko hi'), the parameter update of the unfused path, operation for
+    // operation, to a separate output box, so its next fetch is issued as
+    // soon as chunk g has been computed.  Lane i owns row i of the box, which
+    // is TMEM lane 32q + i; the 64-byte swizzle makes these row reads
+    // conflict-free.
     constexpr bool APPLY = EPI == EPI_APPLY;
+    constexpr bool INPLACE = Layout<EPI>::inplace;
     constexpr int SLOTS = Layout<EPI>::slots;
     constexpr int IN_BYTES = Layout<EPI>::in_bytes;
     const int ew = warp - 2;
@@ -589,8 +633,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t r[32];
         __syncwarp();
         tmem_ld32(taddr + (uint32_t)(ch * 32), r);
-        if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the output box
+        if (!INPLACE && lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the output box
         __syncwarp();
+        uint8_t *ob = INPLACE ? ebuf : obuf;
+        const uint32_t ob_s = INPLACE ? ebase_s + slot * IN_BYTES : obuf_s;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint32_t off = (uint32_t)(lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
@@ -614,15 +660,16 @@ __global__ void __launch_bounds__(THREADS, 1)
               lo.h[e] = __floats2bfloat162_rn(v0 - hh.x, v1 - hh.y);
             }
           }
-          *reinterpret_cast<uint4 *>(obuf + off) = ho.v;
-          if (lo_out) *reinterpret_cast<uint4 *>(obuf + EPI_BOX_BYTES + off) = lo.v;
+          *reinterpret_cast<uint4 *>(ob + off) = ho.v;
+          if (lo_out) *reinterpret_cast<uint4 *>(ob + EPI_BOX_BYTES + off) = lo.v;
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_3d(&p.tm_out, obuf_s, col0, row0, mat);
-          if (lo_out) tma_store_3d(&p.tm_out_lo, obuf_s + EPI_BOX_BYTES, col0, row0, mat);
+          tma_store_3d(&p.tm_out, ob_s, col0, row0, mat);
+          if (lo_out) tma_store_3d(&p.tm_out_lo, ob_s + EPI_BOX_BYTES, col0, row0, mat);
           bulk_commit();
+          if (INPLACE) bulk_wait_read_all();  // the store has read the slot the next load fills
           // every lane has read this input slot: fetch chunk ch + SLOTS into it (possibly of the next tile)
           const int nc = ch + SLOTS;
           if (nc < CHUNKS)
