@@ -283,9 +283,12 @@ def run_gpu(args):
 
         host_p_views = split(host_p)
 
+        host_g_views = split(host_g)
+
         def e2e_steps_fused(n):
-            # step k's gradients arrive in device buffer k % 2, copied in while
-            # step k-1 computes; group j's parameters are copied out while the
+            # step k's gradients arrive in device buffer k % 2, copied in group
+            # by group while step k-1 computes (group j's call waits only for
+            # its own gradients); group j's parameters are copied out while the
             # next group computes, and step k+1's call for group j (which
             # writes its parameters) waits for that copy
             ev_in, ev_used, ev_out = [None, None], [None, None], [None] * len(groups)
@@ -296,17 +299,20 @@ def run_gpu(args):
                     s_in.wait_event(ev_used[i])
                 else:
                     s_in.wait_stream(stream)
-                with torch.cuda.stream(s_in):
-                    grads[i].copy_(host_g, non_blocking=True)
-                ev_in[i] = s_in.record_event()
+                evs = []
+                for j in range(len(groups)):
+                    with torch.cuda.stream(s_in):
+                        g_views[i][j].copy_(host_g_views[j], non_blocking=True)
+                    evs.append(s_in.record_event())
+                ev_in[i] = evs
 
             copy_in(0)
             for k in range(n):
                 i = k % 2
                 if k + 1 < n:
                     copy_in(k + 1)
-                stream.wait_event(ev_in[i])
                 for j, (p, g, m) in enumerate(zip(p_views, g_views[i], m_views)):
+                    stream.wait_event(ev_in[i][j])
                     if ev_out[j] is not None:
                         stream.wait_event(ev_out[j])
                     fused_group(p, g, m)
