@@ -144,6 +144,7 @@ struct Layout {
   // [X hi][X lo][W], output [W'] in a box of its own, so that fetching the
   // next input never waits for the previous store to finish reading.
   static constexpr int in_bytes = (EPI == EPI_APPLY ? 3 : 2) * EPI_BOX_BYTES;
+  static_assert(EPI >= EPI_AXPY || in_bytes == EPI_BUF, "the symmetric epilogues address slots of EPI_BUF bytes");
   static constexpr bool inplace = EPI == EPI_AXPY && MUON_AXPY_INPLACE != 0;
   static constexpr int out_bytes =
       EPI == EPI_APPLY ? EPI_BOX_BYTES : (EPI == EPI_AXPY && !inplace) ? 2 * EPI_BOX_BYTES : 0;
