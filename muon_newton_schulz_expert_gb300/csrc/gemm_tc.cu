@@ -69,6 +69,9 @@ constexpr int UMMA_K = 16;
 //    over it).  aX + BX: one slot of X's halves, the result written over it,
 //    so 3 double stages fit.  aX + BX with the update: three input boxes and
 //    a separate output box, which leaves room for 5 single stages.
+#ifndef MUON_AXPY_ROW_ORDER_T
+#define MUON_AXPY_ROW_ORDER_T 1
+#endif
 #ifndef MUON_AXPY_INPLACE
 #define MUON_AXPY_INPLACE 1
 #endif
@@ -169,6 +172,7 @@ struct Params {
   int M, N, K;                 // output M x N, reduction length K (per matrix)
   int tiles_m, tiles_n;        // pair tiles of 256 x 256
   int tiles_per_mat;
+  int row_order;               // aX + BX: tiles ordered along rows (1) or down columns (0)
   long long num_tiles;
   __nv_bfloat16 *out;
   long long out_ld, out_mat;   // row stride and matrix stride in elements
@@ -359,15 +363,23 @@ __host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool a_mn_major,
 }
 
 // Tile t -> (matrix, row tile, column tile) of 256 x 256 pair tiles.
-// Symmetric outputs enumerate, per matrix, the tiles on or above the
-// diagonal: row tile i needs column tiles j >= i.
+// aX + BX walks the tiles so that consecutive ones (which run at the same
+// time on neighbouring pairs) share their block of X, the operand read by 7
+// tiles: down a column when X is the B operand, along a row when it is the A
+// operand (X stored transposed).  Symmetric outputs enumerate, per matrix,
+// the tiles on or above the diagonal: row tile i needs column tiles j >= i.
 template <int EPI>
 __device__ __forceinline__ void decode_tile(const Params &p, long long t, int &mat, int &ti, int &tj) {
   mat = (int)(t / p.tiles_per_mat);
   int r = (int)(t - (long long)mat * p.tiles_per_mat);
   if (EPI >= EPI_AXPY) {
-    tj = r / p.tiles_m;
-    ti = r - tj * p.tiles_m;
+    if (p.row_order) {
+      ti = r / p.tiles_n;
+      tj = r - ti * p.tiles_n;
+    } else {
+      tj = r / p.tiles_m;
+      ti = r - tj * p.tiles_m;
+    }
   } else {
     int i = 0;
     for (;;) {
@@ -460,12 +472,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int arow = ti * CM + (int)rank * BM;    // this CTA's rows of A
         const int brow = tj * BN + (int)rank * BNH;   // this CTA's half of B
         // aX + BX: tiles that share an operand block start their K loop at
-        // different offsets ((ti + tj) mod T of T segments), so that a
-        // block's first fetch from DRAM is waited on by one tile while the
-        // others read blocks already in L2.  The sum over K starts and wraps
-        // at the offset (a fixed order per tile).  The long-K symmetric
-        // kernels keep the plain order: there the rotation stretched the
-        // reuse distance past what L2 holds and measured slower.
+        // different offsets ((ti + tj) mod T of T segments, T the larger tile
+        // count, so neighbouring tiles start about one k-block apart): a
+        // block's first fetch from DRAM is waited on by the leading tile and
+        // the ones just behind it read it from L2.  The sum over K starts and
+        // wraps at the offset (a fixed order per tile).  Spreading the starts
+        // over the whole K loop (T = 7) measured slower, as did any rotation
+        // in the long-K symmetric kernels (reuse distances past what L2 holds).
         const int kt = p.tiles_m > p.tiles_n ? p.tiles_m : p.tiles_n;
         const int kb0 = EPI >= EPI_AXPY ? (int)((long long)((ti + tj) % kt) * num_kb / kt) : 0;
         bool ok = true;
@@ -1066,6 +1079,7 @@ int axpy_launch(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloa
   p.out_lo = Xn_lo;
   p.kw = kw;
   p.ko = ko;
+  p.row_order = transposed ? MUON_AXPY_ROW_ORDER_T : 0;
   return transposed ? launch<EPI, false, false>(ma, mb, p, trace_kind, s)
                     : launch<EPI, false, true>(ma, mb, p, trace_kind, s);
 }
