@@ -26,8 +26,8 @@
 // shared memory, which is what keeps its bandwidth below the tensor cores'
 // appetite.
 //   warp 0 lane 0  TMA producer (both CTAs): 128x64 bf16 boxes, 128-byte
-//                  swizzle, a ring of 3 two-k-block or 5 one-k-block
-//                  stages (Layout); completion is
+//                  swizzle, a ring of 3 stages of two k-blocks (Layout);
+//                  completion is
 //                  signalled on the even CTA's "full" barrier, which counts
 //                  the bytes of both halves;
 //   warp 1         TMEM allocation of 512 columns (two 128 x 256 fp32
@@ -67,8 +67,14 @@ constexpr int UMMA_K = 16;
 //  - Epilogue slots: one slot = two or three 2 KB boxes per epilogue warp.
 //    X X^T: one slot (output staging).  bA + cAA: one slot (b*A in, result
 //    over it).  aX + BX: one slot of X's halves, the result written over it,
-//    so 3 double stages fit.  aX + BX with the update: three input boxes and
-//    a separate output box, which leaves room for 5 single stages.
+//    so 3 double stages fit.  aX + BX with the update: three input boxes of
+//    16-column chunks (1 KB each), W' written over them, so that 3 double
+//    stages fit there too.
+// aX + BX with the update: 16-column epilogue chunks (1 KB boxes) with W'
+// written over the slot, so that three two-k-block stages fit beside it
+#ifndef MUON_APPLY_CW16
+#define MUON_APPLY_CW16 1
+#endif
 #ifndef MUON_AXPY_ROW_ORDER_T
 #define MUON_AXPY_ROW_ORDER_T 1
 #endif
@@ -85,7 +91,7 @@ constexpr int UMMA_K = 16;
 #define MUON_KSUB_AXPY 2
 #endif
 #ifndef MUON_KSUB_APPLY
-#define MUON_KSUB_APPLY 1
+#define MUON_KSUB_APPLY 2
 #endif
 #ifndef MUON_STAGES_SYRK
 #define MUON_STAGES_SYRK 3
@@ -106,7 +112,7 @@ constexpr int UMMA_K = 16;
 #define MUON_SLOTS_AXPY 1
 #endif
 #ifndef MUON_STAGES_APPLY
-#define MUON_STAGES_APPLY 5
+#define MUON_STAGES_APPLY 3
 #endif
 #ifndef MUON_SLOTS_APPLY
 #define MUON_SLOTS_APPLY 1
@@ -144,13 +150,17 @@ struct Layout {
   // SYRK/POLY: a slot is [direct box][mirror box], with no separate output.
   // AXPY: input [X hi][X lo], the result [X' hi][X' lo] written over it (or,
   // with MUON_AXPY_INPLACE 0, into an output box of its own); APPLY: input
-  // [X hi][X lo][W], output [W'] in a box of its own, so that fetching the
-  // next input never waits for the previous store to finish reading.
-  static constexpr int in_bytes = (EPI == EPI_APPLY ? 3 : 2) * EPI_BOX_BYTES;
+  // [X hi][X lo][W] of 16-column boxes, W' written over it (or, with
+  // MUON_APPLY_CW16 0, 32-column boxes and W' in a box of its own, so that
+  // fetching the next input never waits for the previous store to read).
+  // epilogue chunk width in columns (boxes of 32 rows x cw)
+  static constexpr int cw = (EPI == EPI_APPLY && MUON_APPLY_CW16) ? 16 : 32;
+  static constexpr int box_bytes = 32 * cw * 2;
+  static constexpr int in_bytes = (EPI == EPI_APPLY ? 3 : 2) * box_bytes;
   static_assert(EPI >= EPI_AXPY || in_bytes == EPI_BUF, "the symmetric epilogues address slots of EPI_BUF bytes");
-  static constexpr bool inplace = EPI == EPI_AXPY && MUON_AXPY_INPLACE != 0;
-  static constexpr int out_bytes =
-      EPI == EPI_APPLY ? EPI_BOX_BYTES : (EPI == EPI_AXPY && !inplace) ? 2 * EPI_BOX_BYTES : 0;
+  static constexpr bool inplace =
+      (EPI == EPI_AXPY && MUON_AXPY_INPLACE != 0) || (EPI == EPI_APPLY && MUON_APPLY_CW16 != 0);
+  static constexpr int out_bytes = inplace ? 0 : EPI == EPI_APPLY ? box_bytes : EPI == EPI_AXPY ? 2 * box_bytes : 0;
   static constexpr int epi_bytes = EPI_WARPS * (slots * in_bytes + out_bytes);
   static constexpr int num_bars = 2 * stages + 5 + EPI_WARPS * slots;
   // k-blocks of 64 per stage (one barrier round trip per ksub k-blocks)
@@ -160,7 +170,7 @@ struct Layout {
                                                 : MUON_KSUB_SYRK;
   static constexpr int stage_bytes = ksub * STAGE_BYTES;
   static constexpr int smem_bytes = stages * stage_bytes + epi_bytes + 1024 + num_bars * 8 + 16;
-  static_assert(CHUNKS % slots == 0, "chunks per tile must fill the staging slots evenly");
+  static_assert((128 / cw) % slots == 0, "chunks per tile must fill the staging slots evenly");
   static_assert(smem_bytes <= 232448, "shared memory per CTA");
 };
 
@@ -334,6 +344,17 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
 }
 
 // 32 lanes x 32 consecutive fp32 columns -> 32 registers per thread, waited.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -586,14 +607,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     // boxes of chunk g + SLOTS are fetched into the slot once that store has
     // read it.  APPLY also stages the box of W and writes W' = bf16(kw W +
     // ko hi'), the parameter update of the unfused path, operation for
-    // operation, to a separate output box, so its next fetch is issued as
-    // soon as chunk g has been computed.  Lane i owns row i of the box, which
-    // is TMEM lane 32q + i; the 64-byte swizzle makes these row reads
-    // conflict-free.
+    // operation, over the slot, in chunks of 16 columns (three 1 KB boxes) so
+    // that the ring keeps three double stages.  Lane i owns row i of the box,
+    // which is TMEM lane 32q + i; the swizzle spanning a box row (64 or 32
+    // bytes) makes these row reads conflict-free.
     constexpr bool APPLY = EPI == EPI_APPLY;
     constexpr bool INPLACE = Layout<EPI>::inplace;
     constexpr int SLOTS = Layout<EPI>::slots;
     constexpr int IN_BYTES = Layout<EPI>::in_bytes;
+    constexpr int CW = Layout<EPI>::cw;            // chunk width: 32 columns, or 16
+    constexpr int NCH = 128 / CW;                  // chunks per warp and tile
+    constexpr int BOXB = Layout<EPI>::box_bytes;   // one 32 x CW box
+    constexpr int PIECES = CW / 8;                 // 16-byte pieces per box row
     const int ew = warp - 2;
     const int q = warp & 3, half = ew >> 2;
     // SLOTS input slots, then the output slot
@@ -603,14 +628,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t obuf_s = ebase_s + SLOTS * IN_BYTES;
     uint32_t ephase_bits = 0;                                // parity per slot
     const bool lo_in = p.src_lo != nullptr, lo_out = !APPLY && p.out_lo != nullptr;
-    const uint32_t etx = (lo_in ? 2u : 1u) * EPI_BOX_BYTES + (APPLY ? (uint32_t)EPI_BOX_BYTES : 0u);
+    const uint32_t etx = (lo_in ? 2u : 1u) * BOXB + (APPLY ? (uint32_t)BOXB : 0u);
     auto epi_load = [&](int slot, int m_, int row0_, int col0_) {  // lane 0 only
       const uint32_t dst = ebase_s + slot * IN_BYTES, bar = EBAR(ew * SLOTS + slot);
       fence_proxy_async_smem();
       mbar_expect_tx(bar, etx);
       tma_load_3d(dst, &p.tm_src, bar, col0_, row0_, m_);
-      if (lo_in) tma_load_3d(dst + EPI_BOX_BYTES, &p.tm_src_lo, bar, col0_, row0_, m_);
-      if (APPLY) tma_load_3d(dst + 2 * EPI_BOX_BYTES, &p.tm_out, bar, col0_, row0_, m_);  // W, stored over later
+      if (lo_in) tma_load_3d(dst + BOXB, &p.tm_src_lo, bar, col0_, row0_, m_);
+      if (APPLY) tma_load_3d(dst + 2 * BOXB, &p.tm_out, bar, col0_, row0_, m_);  // W, stored over later
     };
     const int rbase = (int)rank * BM + q * 32;  // this warp's rows within a pair tile
     int acc = 0;
@@ -620,7 +645,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (t < p.num_tiles) {
       decode_tile<EPI>(p, t, mat, ti, tj);
       if (lane == 0)
-        for (int c = 0; c < SLOTS; ++c) epi_load(c, mat, ti * CM + rbase, tj * BN + half * 128 + c * 32);
+        for (int c = 0; c < SLOTS; ++c) epi_load(c, mat, ti * CM + rbase, tj * BN + half * 128 + c * CW);
     }
     bool alive = true;
     for (; alive && t < p.num_tiles; t += ncl) {
@@ -634,10 +659,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS + half * 128);
       const float sc = p.scale ? p.scale[mat] : 1.0f;
 #pragma unroll 1
-      for (int ch = 0; ch < CHUNKS; ++ch) {
-        const int slot = ch % SLOTS;   // CHUNKS is a multiple of SLOTS
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int slot = ch % SLOTS;   // NCH is a multiple of SLOTS
         uint8_t *ebuf = ebase + slot * IN_BYTES;
-        const int col0 = tj * BN + half * 128 + ch * 32;
+        const int col0 = tj * BN + half * 128 + ch * CW;
         const bool got = wait_bounded(EBAR(ew * SLOTS + slot), (ephase_bits >> slot) & 1u, w);
         if (!__all_sync(0xffffffffu, got)) {
           alive = false;
@@ -646,18 +671,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         ephase_bits ^= 1u << slot;
         uint32_t r[32];
         __syncwarp();
-        tmem_ld32(taddr + (uint32_t)(ch * 32), r);
+        if (CW == 32)
+          tmem_ld32(taddr + (uint32_t)(ch * CW), r);
+        else
+          tmem_ld16(taddr + (uint32_t)(ch * CW), r);
         if (!INPLACE && lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the output box
         __syncwarp();
         uint8_t *ob = INPLACE ? ebuf : obuf;
         const uint32_t ob_s = INPLACE ? ebase_s + slot * IN_BYTES : obuf_s;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t off = (uint32_t)(lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
+        for (int c = 0; c < PIECES; ++c) {
+          // 64-byte rows with the 64-byte swizzle, or 32-byte rows with the 32-byte swizzle
+          const uint32_t off = CW == 32 ? (uint32_t)(lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4))
+                                        : (uint32_t)(lane * 32 + ((c ^ ((lane >> 2) & 1)) << 4));
           Pack8 hv, lv, wv, ho, lo;
           hv.v = *reinterpret_cast<const uint4 *>(ebuf + off);
-          lv.v = lo_in ? *reinterpret_cast<const uint4 *>(ebuf + EPI_BOX_BYTES + off) : make_uint4(0u, 0u, 0u, 0u);
-          if (APPLY) wv.v = *reinterpret_cast<const uint4 *>(ebuf + 2 * EPI_BOX_BYTES + off);
+          lv.v = lo_in ? *reinterpret_cast<const uint4 *>(ebuf + BOXB + off) : make_uint4(0u, 0u, 0u, 0u);
+          if (APPLY) wv.v = *reinterpret_cast<const uint4 *>(ebuf + 2 * BOXB + off);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int k = c * 8 + 2 * e;
@@ -675,21 +705,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
           *reinterpret_cast<uint4 *>(ob + off) = ho.v;
-          if (lo_out) *reinterpret_cast<uint4 *>(ob + EPI_BOX_BYTES + off) = lo.v;
+          if (lo_out) *reinterpret_cast<uint4 *>(ob + BOXB + off) = lo.v;
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           tma_store_3d(&p.tm_out, ob_s, col0, row0, mat);
-          if (lo_out) tma_store_3d(&p.tm_out_lo, ob_s + EPI_BOX_BYTES, col0, row0, mat);
+          if (lo_out) tma_store_3d(&p.tm_out_lo, ob_s + BOXB, col0, row0, mat);
           bulk_commit();
           if (INPLACE) bulk_wait_read_all();  // the store has read the slot the next load fills
           // every lane has read this input slot: fetch chunk ch + SLOTS into it (possibly of the next tile)
           const int nc = ch + SLOTS;
-          if (nc < CHUNKS)
-            epi_load(slot, mat, row0, col0 + SLOTS * 32);
+          if (nc < NCH)
+            epi_load(slot, mat, row0, col0 + SLOTS * CW);
           else if (tn < p.num_tiles)
-            epi_load(slot, mat_n, ti_n * CM + rbase, tj_n * BN + half * 128 + (nc - CHUNKS) * 32);
+            epi_load(slot, mat_n, ti_n * CM + rbase, tj_n * BN + half * 128 + (nc - NCH) * CW);
         }
         __syncwarp();
       }
@@ -1058,13 +1088,14 @@ int axpy_launch(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloa
     p.out_ld = m;
   }
   if (st) return st;
-  // epilogue boxes over X, X_lo, Xn, Xn_lo, all stored p.M x p.N
-  const int eb = EPI_BOX;
-  const CUtensorMapSwizzle sw64 = CU_TENSOR_MAP_SWIZZLE_64B;
-  st = make_map(&p.tm_src, X, batch, p.M, p.N, eb, eb, sw64);
-  if (!st && X_lo) st = make_map(&p.tm_src_lo, X_lo, batch, p.M, p.N, eb, eb, sw64);
-  if (!st) st = make_map(&p.tm_out, Xn, batch, p.M, p.N, eb, eb, sw64);
-  if (!st && Xn_lo) st = make_map(&p.tm_out_lo, Xn_lo, batch, p.M, p.N, eb, eb, sw64);
+  // epilogue boxes over X, X_lo, Xn, Xn_lo, all stored p.M x p.N: 32 rows x cw
+  // columns, the swizzle spanning one box row
+  const int eb = EPI_BOX, ecw = Layout<EPI>::cw;
+  const CUtensorMapSwizzle sw64 = ecw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  st = make_map(&p.tm_src, X, batch, p.M, p.N, eb, ecw, sw64);
+  if (!st && X_lo) st = make_map(&p.tm_src_lo, X_lo, batch, p.M, p.N, eb, ecw, sw64);
+  if (!st) st = make_map(&p.tm_out, Xn, batch, p.M, p.N, eb, ecw, sw64);
+  if (!st && Xn_lo) st = make_map(&p.tm_out_lo, Xn_lo, batch, p.M, p.N, eb, ecw, sw64);
   if (st) return st;
   p.tiles_per_mat = p.tiles_m * p.tiles_n;
   p.num_tiles = (long long)p.tiles_per_mat * batch;
