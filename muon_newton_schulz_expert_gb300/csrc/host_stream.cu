@@ -11,8 +11,8 @@
 // two device slots.  For chunk k (slot k % 2):
 //   copy-in stream   waits until slot k%2's previous chunk has been copied out,
 //                    then copies gradients, momentum and parameters in;
-//   caller's stream  waits for the copy-in, runs momentum -> Newton-Schulz ->
-//                    update on the slot;
+//   caller's stream  waits for the copy-in, runs the fused step (momentum ->
+//                    Newton-Schulz -> update, muon_step_batched) on the slot;
 //   copy-out stream  waits for the compute, copies parameters and momentum out.
 // Copies of chunk k+1 and k-1 therefore overlap the compute of chunk k.  The
 // caller's stream finally waits for the last copy-out, so completion of the
@@ -80,8 +80,8 @@ extern "C" int muon_step_host(void *param_host, const void *grad_host, float *mo
   const int64_t per = rows * cols;
   const int64_t ch = chunk > 0 ? std::min(chunk, batch) : std::min<int64_t>(batch, 8);
   const size_t g_bytes = align256((size_t)ch * per * 2), m_bytes = align256((size_t)ch * per * 4);
-  const size_t slot_bytes = 3 * g_bytes + m_bytes;  // grad, param, u (bf16) + momentum (fp32)
-  const size_t ws = muon_ns_workspace_bytes(ch, rows, cols);
+  const size_t slot_bytes = 2 * g_bytes + m_bytes;  // grad, param (bf16) + momentum (fp32)
+  const size_t ws = muon_step_workspace_bytes(ch, rows, cols);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   Streams st;
@@ -108,8 +108,8 @@ extern "C" int muon_step_host(void *param_host, const void *grad_host, float *mo
     const int slot = (int)(k & 1);
     const int64_t nb = std::min(ch, batch - b0);
     uint8_t *base = dev + slot * slot_bytes;
-    auto *g_d = base, *p_d = base + g_bytes, *u_d = base + 2 * g_bytes;
-    auto *m_d = reinterpret_cast<float *>(base + 3 * g_bytes);
+    auto *g_d = base, *p_d = base + g_bytes;
+    auto *m_d = reinterpret_cast<float *>(base + 2 * g_bytes);
     const size_t gb = (size_t)nb * per * 2, mb = (size_t)nb * per * 4;
     const size_t go = (size_t)b0 * per * 2, mo = (size_t)b0 * per * 4;
     // copy in (after this slot's previous chunk has been copied out)
@@ -123,10 +123,8 @@ extern "C" int muon_step_host(void *param_host, const void *grad_host, float *mo
     }
     // compute on the caller's stream
     cudaStreamWaitEvent(s, st.in_done[slot], 0);
-    status = muon_momentum_update(g_d, m_d, u_d, nb * per, mu, nesterov, stream);
-    if (status == MUON_OK)
-      status = muon_ns_batched_ws(u_d, nb, rows, cols, steps, coeffs, eps, dev + 2 * slot_bytes, ws, stream);
-    if (status == MUON_OK) status = muon_apply_update(p_d, u_d, nb, rows, cols, lr, weight_decay, scale, stream);
+    status = muon_step_batched(p_d, g_d, m_d, nb, rows, cols, mu, nesterov, steps, coeffs, eps, lr, weight_decay,
+                               scale, dev + 2 * slot_bytes, ws, stream);
     if (status != MUON_OK) break;
     cudaEventRecord(st.compute_done[slot], s);
     // copy out
