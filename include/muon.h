@@ -199,6 +199,16 @@ int muon_step_batched(void *param, const void *grad, float *momentum, int64_t ba
                       float weight_decay, float scale, void *workspace, size_t workspace_bytes,
                       muon_stream_t stream);
 
+/* The fused step with one (a, b, c) row per Newton-Schulz step: coeffs is a
+ * host array of 3*steps floats as in muon_ns_batched_schedule (any non-null
+ * pointer when steps == 0).  Bit for bit muon_momentum_update ->
+ * muon_ns_batched_schedule -> muon_apply_update; everything else as
+ * muon_step_batched. */
+int muon_step_batched_schedule(void *param, const void *grad, float *momentum, int64_t batch, int64_t rows,
+                               int64_t cols, float mu, int nesterov, int steps, const float *coeffs, float eps,
+                               float lr, float weight_decay, float scale, void *workspace, size_t workspace_bytes,
+                               muon_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * The whole Muon step on matrices that live in host memory (FlexShard
  * section: with the parameters offloaded to host memory, Newton-Schulz runs on

@@ -62,6 +62,8 @@ SIGNATURES = {
     "muon_default_scale": (_F, [_I64, _I64]),
     "muon_step_workspace_bytes": (_SIZE, [_I64, _I64, _I64]),
     "muon_step_batched": (_INT, [_P, _P, _P, _I64, _I64, _I64, _F, _INT, _INT, _P, _F, _F, _F, _F, _P, _SIZE, _P]),
+    "muon_step_batched_schedule": (_INT, [_P, _P, _P, _I64, _I64, _I64, _F, _INT, _INT, _P, _F, _F, _F, _F, _P, _SIZE,
+                                          _P]),
     "muon_step_host": (_INT, [_P, _P, _P, _I64, _I64, _I64, _F, _INT, _INT, _P, _F, _F, _F, _F, _I64, _P]),
     "muon_adamw_update": (_INT, [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P]),
     "muon_adamw_update_f32": (_INT, [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P]),
@@ -330,6 +332,26 @@ def muon_step_batched(param, grad, momentum, *, mu=0.95, nesterov=True, steps=5,
         _ptr(param), _ptr(grad), _ptr(momentum), b, r, c, float(mu), int(bool(nesterov)), int(steps),
         _coeffs(coeffs), float(eps), float(lr), float(weight_decay), float(scale), ws, ws_bytes,
         _stream_handle(stream)))
+
+
+def muon_step_batched_schedule(param, grad, momentum, coeff_rows, *, mu=0.95, nesterov=True, eps=1e-7, lr=0.02,
+                               weight_decay=0.1, scale=0.0, workspace=None, stream=None):
+    """muon_step_batched with one (a, b, c) row per Newton-Schulz step (in place)."""
+    import torch
+    _need(param, torch.bfloat16, "param")
+    _need(grad, torch.bfloat16, "grad")
+    _need(momentum, torch.float32, "momentum")
+    if not (param.shape == grad.shape == momentum.shape):
+        raise ValueError("param, grad and momentum must have the same shape")
+    b, r, c = _bmn(param)
+    steps, arr = _schedule(coeff_rows)
+    ws, ws_bytes = None, 0
+    if workspace is not None:
+        _need(workspace, torch.uint8, "workspace")
+        ws, ws_bytes = _ptr(workspace), workspace.numel()
+    _check("muon_step_batched_schedule", lib().muon_step_batched_schedule(
+        _ptr(param), _ptr(grad), _ptr(momentum), b, r, c, float(mu), int(bool(nesterov)), steps, arr, float(eps),
+        float(lr), float(weight_decay), float(scale), ws, ws_bytes, _stream_handle(stream)))
 
 
 def muon_step_host(param_host, grad_host, momentum_host, *, mu=0.95, nesterov=True, steps=5, coeffs=QUINTIC,

@@ -431,8 +431,8 @@ size_t muon_step_workspace_bytes(int64_t batch, int64_t rows, int64_t cols) {
 // u lives in the second X buffer, which the rotation first writes in
 // iteration 2, after iteration 1 has read u for the last time.
 static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, const Workspace &w, int64_t batch,
-                      int64_t rows, int64_t cols, float mu, int nesterov, int steps, const float *cf, float eps,
-                      float kw, float ko, cudaStream_t s) {
+                      int64_t rows, int64_t cols, float mu, int nesterov, int steps, const float *cf0,
+                      int cf_stride, float eps, float kw, float ko, cudaStream_t s) {
   const int64_t mm = std::min(rows, cols), nn = std::max(rows, cols), per = rows * cols;
   const bool transposed = rows > cols;
   auto *x1 = static_cast<__nv_bfloat16 *>(w.x1);
@@ -447,6 +447,7 @@ static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, cons
   }
   __nv_bfloat16 *src = x2;
   for (int it = 0; it < steps; ++it) {
+    const float *cf = cf0 + (size_t)it * cf_stride;
     MUON_TRY(ns_syrk(src, A, batch, mm, nn, it == 0 ? w.inv2 : nullptr, transposed, s));
     MUON_TRY(ns_poly(A, B, batch, mm, cf[1], cf[2], s));
     const __nv_bfloat16 *src_lo = it == 0 ? nullptr : lo;
@@ -460,11 +461,12 @@ static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, cons
   return MUON_OK;
 }
 
-int muon_step_batched(void *param, const void *grad, float *momentum, int64_t batch, int64_t rows, int64_t cols,
-                      float mu, int nesterov, int steps, const float coeffs[3], float eps, float lr,
-                      float weight_decay, float scale, void *workspace, size_t workspace_bytes,
-                      muon_stream_t stream) {
-  MUON_TRY(check_ns_args(param, batch, rows, cols, steps, coeffs, eps));
+// Checked arguments of both fused-step calls; cf holds (a, b, c) for step it
+// at cf + it * cf_stride.
+static int step_fused_entry(void *param, const void *grad, float *momentum, int64_t batch, int64_t rows, int64_t cols,
+                            float mu, int nesterov, int steps, const float *cf, int cf_stride, float eps, float lr,
+                            float weight_decay, float scale, void *workspace, size_t workspace_bytes,
+                            cudaStream_t s) {
   if (!isfinite(mu) || !isfinite(lr) || !isfinite(weight_decay) || !isfinite(scale)) return MUON_ERR_INVALID_ARG;
   if (batch == 0) return MUON_OK;
   if (!grad || !momentum) return MUON_ERR_INVALID_ARG;
@@ -475,19 +477,38 @@ int muon_step_batched(void *param, const void *grad, float *momentum, int64_t ba
   const size_t need = ws_bytes(batch, mm, nn, 2);
   if (workspace && workspace_bytes < need) return MUON_ERR_NO_MEMORY;
   if (!device_error_word()) return MUON_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float kw, ko;
   update_constants(rows, cols, lr, weight_decay, scale, &kw, &ko);
-  const float cf[3] = {coeffs[0], coeffs[1], coeffs[2]};
   void *ws = workspace;
   if (!ws && (cudaMallocAsync(&ws, need, s) != cudaSuccess || !ws)) {
     cudaGetLastError();
     return MUON_ERR_NO_MEMORY;
   }
   int st = step_fused(static_cast<__nv_bfloat16 *>(param), static_cast<const __nv_bfloat16 *>(grad), momentum,
-                      carve(ws, batch, mm, nn, 2), batch, rows, cols, mu, nesterov ? 1 : 0, steps, cf, eps, kw, ko, s);
+                      carve(ws, batch, mm, nn, 2), batch, rows, cols, mu, nesterov ? 1 : 0, steps, cf, cf_stride, eps,
+                      kw, ko, s);
   if (!workspace && cudaFreeAsync(ws, s) != cudaSuccess && st == MUON_OK) st = MUON_ERR_CUDA;
   return st;
+}
+
+int muon_step_batched(void *param, const void *grad, float *momentum, int64_t batch, int64_t rows, int64_t cols,
+                      float mu, int nesterov, int steps, const float coeffs[3], float eps, float lr,
+                      float weight_decay, float scale, void *workspace, size_t workspace_bytes,
+                      muon_stream_t stream) {
+  MUON_TRY(check_ns_args(param, batch, rows, cols, steps, coeffs, eps));
+  const float cf[3] = {coeffs[0], coeffs[1], coeffs[2]};
+  return step_fused_entry(param, grad, momentum, batch, rows, cols, mu, nesterov, steps, cf, 0, eps, lr, weight_decay,
+                          scale, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int muon_step_batched_schedule(void *param, const void *grad, float *momentum, int64_t batch, int64_t rows,
+                               int64_t cols, float mu, int nesterov, int steps, const float *coeffs, float eps,
+                               float lr, float weight_decay, float scale, void *workspace, size_t workspace_bytes,
+                               muon_stream_t stream) {
+  MUON_TRY(check_ns_args(param, batch, rows, cols, steps, coeffs, eps, 3 * (int64_t)steps));
+  std::vector<float> cf(coeffs, coeffs + 3 * (size_t)steps);
+  return step_fused_entry(param, grad, momentum, batch, rows, cols, mu, nesterov, steps, cf.data(), 3, eps, lr,
+                          weight_decay, scale, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 static int adamw_consts(float lr, float beta1, float beta2, float eps, float wd, int64_t step, AdamWConsts *k) {

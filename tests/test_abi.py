@@ -150,6 +150,17 @@ def test_newer_entry_points_reject_bad_arguments_on_the_host(lib):
     assert lib.muon_step_batched(P, P, P, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, ctypes.c_void_p(272),
                                  1 << 20, None) == -1      # workspace not 256-byte aligned
     assert lib.muon_step_batched(P, P, P, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, P, 64, None) == -4
+    sched2 = (ctypes.c_float * 6)(3.4445, -4.775, 2.0315, 3.0, -3.2, 1.2)
+    assert lib.muon_step_batched_schedule(None, None, None, 0, 8, 8, 0.95, 1, 2, sched2, 1e-7, 0.02, 0.1, 0.0, None, 0,
+                                          None) == 0
+    assert lib.muon_step_batched_schedule(P, P, P, 1, 8, 8, 0.95, 1, 2, None, 1e-7, 0.02, 0.1, 0.0, None, 0,
+                                          None) == -1
+    assert lib.muon_step_batched_schedule(P, P, P, 1, 8, 8, 0.95, 1, 2, sched, 1e-7, 0.02, 0.1, 0.0, None, 0,
+                                          None) == -1      # a NaN coefficient in step 2
+    assert lib.muon_step_batched_schedule(P, P, P, 1, 12, 8, 0.95, 1, 2, sched2, 1e-7, 0.02, 0.1, 0.0, None, 0,
+                                          None) == -2
+    assert lib.muon_step_batched_schedule(P, P, P, 1, 8, 8, 0.95, 1, 2, sched2, 1e-7, 0.02, 0.1, 0.0, P, 64,
+                                          None) == -4
     assert lib.muon_step_workspace_bytes(96, 6144, 1792) == lib.muon_ns_workspace_bytes(96, 1792, 6144)
     assert lib.muon_step_workspace_bytes(0, 8, 8) == 0
 

@@ -121,6 +121,29 @@ def test_fused_step_at_bench_size_equals_separate_calls(mk):
         torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("count,rows,cols", [(3, 256, 768), (2, 776, 264)])
+def test_fused_schedule_equals_separate_calls(mk, count, rows, cols):
+    rows_ = [O.QUINTIC, (3.0, -3.2, 1.2), O.QUINTIC, (2.0, -1.5, 0.5)]
+    g, W, buf = _inputs(count, rows, cols, 960 + rows)
+    W1, b1, u = W.clone(), buf.clone(), torch.empty_like(g)
+    mk.muon_momentum_update(g, b1, u, 0.95, True)
+    mk.muon_ns_batched_schedule(u, rows_, 1e-7)
+    mk.muon_apply_update(W1, u, 0.02, 0.1, 0.0)
+    W2, b2 = W.clone(), buf.clone()
+    mk.muon_step_batched_schedule(W2, g, b2, rows_)
+    torch.cuda.synchronize()
+    assert mk.muon_get_device_status() == 0
+    assert not torch.equal(W1, W)
+    assert np.array_equal(bits32(b2), bits32(b1))
+    assert np.array_equal(bits16(W2), bits16(W1))
+    # a schedule of equal rows is the constant-coefficient step
+    W3, b3, W4, b4 = W.clone(), buf.clone(), W.clone(), buf.clone()
+    mk.muon_step_batched_schedule(W3, g, b3, [O.QUINTIC] * 5)
+    mk.muon_step_batched(W4, g, b4)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits16(W3), bits16(W4))
+
+
 def test_fused_step_launches_its_own_kernels(mk):
     g, W, buf = _inputs(2, 256, 512, 990)
     mk.muon_trace_begin()
