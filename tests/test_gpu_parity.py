@@ -101,16 +101,16 @@ def test_ns_f32_matches_oracle(mk, count, m, n):
     assert rel_fro(np32(X), want) < F32_TOL
 
 
-def test_config1_step_f32(mk):
-    cfg = workloads.CONFIGS[1]
+def test_tiny_f32_step(mk):
+    cfg = workloads.WORKLOADS["tiny_f32_8x64x256"]
     grp = cfg.groups[0]
     dev = "cuda"
-    W = workloads.parameters(grp.count, grp.rows, grp.cols, workloads.seed_for(1, 0, 0, 1), device=dev,
+    W = workloads.parameters(grp.count, grp.rows, grp.cols, workloads.seed_for(cfg.index, 0, 0, 1), device=dev,
                              dtype=torch.float32)
     buf = torch.zeros_like(W)
     u = torch.empty_like(W)
     for step in range(cfg.steps):
-        g = workloads.gradients(grp.count, grp.rows, grp.cols, workloads.seed_for(1, step, 0, 0), device=dev,
+        g = workloads.gradients(grp.count, grp.rows, grp.cols, workloads.seed_for(cfg.index, step, 0, 0), device=dev,
                                 kind="normal", dtype=torch.float32)
         ref = O.muon_step(np32(W), np32(g), np32(buf), mu=f32(0.95), lr=f32(0.02), weight_decay=f32(0.1), bf16=False)
         mk.muon_momentum_update_f32(g, buf, u, mu=0.95)

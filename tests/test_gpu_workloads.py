@@ -29,11 +29,11 @@ def mk():
     return require_gpu()
 
 
-def step_groups(mk, cfg_index, groups, W, buf, u, step):
+def step_groups(mk, wl, groups, W, buf, u, step):
     grads = []
     for gi, grp in enumerate(groups):
-        g = workloads.gradients(grp.count, grp.rows, grp.cols, workloads.seed_for(cfg_index, step, gi, 0),
-                                device="cuda", kind=workloads.CONFIGS[cfg_index].grad_kind)
+        g = workloads.gradients(grp.count, grp.rows, grp.cols, workloads.seed_for(wl.index, step, gi, 0),
+                                device="cuda", kind=wl.grad_kind)
         grads.append(g)
     snap = [(np32(w), np32(b)) for w, b in zip(W, buf)]
     for gi in range(len(groups)):
@@ -67,38 +67,38 @@ def check_matrix(g, W_prev, b_prev, buf_new, u_in, O_gpu, W_new, rows, cols):
     return err
 
 
-def test_config2_one_expert_three_steps(mk):
-    cfg = workloads.CONFIGS[2]
+def test_one_expert_three_steps(mk):
+    cfg = workloads.WORKLOADS["one_expert_w1w3w2"]
     groups = cfg.groups
-    W = [workloads.parameters(g.count, g.rows, g.cols, workloads.seed_for(2, 0, gi, 1), device="cuda")
+    W = [workloads.parameters(g.count, g.rows, g.cols, workloads.seed_for(cfg.index, 0, gi, 1), device="cuda")
          for gi, g in enumerate(groups)]
     buf = [torch.zeros(g.count, g.rows, g.cols, device="cuda") for g in groups]
     u = [torch.empty(g.count, g.rows, g.cols, dtype=torch.bfloat16, device="cuda") for g in groups]
     errs = []
     for step in range(cfg.steps):
-        grads, snap, u_in = step_groups(mk, 2, groups, W, buf, u, step)
+        grads, snap, u_in = step_groups(mk, cfg, groups, W, buf, u, step)
         for gi, grp in enumerate(groups):
             for i in range(grp.count):
                 errs.append(check_matrix(grads[gi][i], snap[gi][0][i], snap[gi][1][i], buf[gi][i], u_in[gi][i],
                                          u[gi][i], W[gi][i], grp.rows, grp.cols))
-    print("config2 rel errors", ["%.3e" % e for e in errs])
+    print("one_expert_w1w3w2 rel errors", ["%.3e" % e for e in errs])
 
 
-def test_config3_rank_batch_sampled(mk):
-    cfg = workloads.CONFIGS[3]
+def test_rank_expert_batch_96_sampled(mk):
+    cfg = workloads.WORKLOADS["rank_expert_batch_96"]
     groups = cfg.groups
-    W = [workloads.parameters(g.count, g.rows, g.cols, workloads.seed_for(3, 0, gi, 1), device="cuda")
+    W = [workloads.parameters(g.count, g.rows, g.cols, workloads.seed_for(cfg.index, 0, gi, 1), device="cuda")
          for gi, g in enumerate(groups)]
     buf = [torch.zeros(g.count, g.rows, g.cols, device="cuda") for g in groups]
     u = [torch.empty(g.count, g.rows, g.cols, dtype=torch.bfloat16, device="cuda") for g in groups]
-    grads, snap, u_in = step_groups(mk, 3, groups, W, buf, u, 0)
+    grads, snap, u_in = step_groups(mk, cfg, groups, W, buf, u, 0)
     samples = {0: (0, 37, 63), 1: (0, 31)}
     for gi, idx in samples.items():
         grp = groups[gi]
         for i in idx:
             err = check_matrix(grads[gi][i], snap[gi][0][i], snap[gi][1][i], buf[gi][i], u_in[gi][i], u[gi][i],
                                W[gi][i], grp.rows, grp.cols)
-            print(f"config3 group {gi} matrix {i}: rel {err:.3e}")
+            print(f"rank_expert_batch_96 group {gi} matrix {i}: rel {err:.3e}")
     # every matrix of the batch: finite and of the quintic's scale (||O||_F^2 / m within the map's range)
     for gi, grp in enumerate(groups):
         m = min(grp.rows, grp.cols)
@@ -106,10 +106,10 @@ def test_config3_rank_batch_sampled(mk):
         assert torch.isfinite(fro2).all() and (fro2 > 0.3).all() and (fro2 < 1.3).all()
 
 
-def test_config4_dense_projections_sampled(mk):
-    cfg = workloads.CONFIGS[4]
+def test_dense_projections_sampled(mk):
+    cfg = workloads.WORKLOADS["dense_projections"]
     groups = cfg.groups
-    X = [workloads.gradients(g.count, g.rows, g.cols, workloads.seed_for(4, 0, gi, 0), device="cuda", kind="normal")
+    X = [workloads.gradients(g.count, g.rows, g.cols, workloads.seed_for(cfg.index, 0, gi, 0), device="cuda", kind="normal")
          for gi, g in enumerate(groups)]
     X_in = [x.clone() for x in X]
     for x in X:
@@ -118,12 +118,12 @@ def test_config4_dense_projections_sampled(mk):
     for gi, i in ((0, 5), (1, 2)):
         want = O.newton_schulz(np32(X_in[gi][i]))
         err = rel_fro(np32(X[gi][i]), want)
-        print(f"config4 group {gi} matrix {i}: rel {err:.3e}")
+        print(f"dense_projections group {gi} matrix {i}: rel {err:.3e}")
         assert err < BF16_TOL
 
 
-def test_config5_conditioning_stress_sampled(mk):
-    cfg = workloads.CONFIGS[5]
+def test_conditioning_stress_128_sampled(mk):
+    cfg = workloads.WORKLOADS["conditioning_stress_128"]
     grp = cfg.groups[0]
     m, n = grp.rows, grp.cols
     G = workloads.spectrum_batch(grp.count, m, n, device="cuda", dtype=torch.float32)
@@ -136,7 +136,7 @@ def test_config5_conditioning_stress_sampled(mk):
         want = O.newton_schulz(np32(G_in[i]))
         got = np32(G[i])
         err = rel_fro(got, want)
-        print(f"config5 matrix {i}: rel {err:.3e}")
+        print(f"conditioning_stress_128 matrix {i}: rel {err:.3e}")
         assert err < BF16_TOL
         # the output singular values follow the scalar quintic map on the known spectrum
         U, s, V = workloads.spectrum_factors(m, n, i, device="cuda", dtype=torch.float32)

@@ -393,10 +393,10 @@ def test_workload_shapes_follow_the_pages():
     assert workloads.HIDDEN == facts["hidden"]
     assert workloads.EXPERT_HIDDEN == facts["expert_hidden"]
     assert workloads.ROUTED_EXPERTS == facts["routed_experts"]
-    c3 = workloads.CONFIGS[3]
-    shapes = {(g.rows, g.cols) for g in c3.groups}
+    batch = workloads.WORKLOADS["rank_expert_batch_96"]
+    shapes = {(g.rows, g.cols) for g in batch.groups}
     assert shapes == {(facts["hidden"], facts["expert_hidden"]), (facts["expert_hidden"], facts["hidden"])}
-    assert sum(g.count for g in c3.groups) == 96   # 32 experts x (w1, w3, w2)
+    assert sum(g.count for g in batch.groups) == 96   # 32 experts x (w1, w3, w2)
 
 
 # --------------------------------------------------------------------------

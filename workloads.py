@@ -40,30 +40,30 @@ class Group:
 
 
 @dataclasses.dataclass(frozen=True)
-class Config:
-    index: int
+class Workload:
+    index: int          # enters the seeds (seed_for)
     name: str
     groups: tuple
     dtype: str          # "bf16" or "f32"
     grad_kind: str      # "lognormal_rows", "normal" or "spectrum"
-    steps: int          # optimizer steps the config is run for
+    steps: int          # optimizer steps the workload is run for
 
 
-CONFIGS = {
-    1: Config(1, "tiny_f32_8x64x256", (Group(8, 64, 256),), "f32", "normal", 3),
-    2: Config(2, "one_expert_w1w3w2", (Group(2, HIDDEN, EXPERT_HIDDEN), Group(1, EXPERT_HIDDEN, HIDDEN)),
-              "bf16", "lognormal_rows", 3),
-    3: Config(3, "rank_expert_batch_96", (Group(64, HIDDEN, EXPERT_HIDDEN), Group(32, EXPERT_HIDDEN, HIDDEN)),
-              "bf16", "lognormal_rows", 1),
-    4: Config(4, "dense_projections", (Group(8, HIDDEN, HIDDEN), Group(4, HIDDEN, 1024)), "bf16", "normal", 1),
-    5: Config(5, "conditioning_stress_128", (Group(128, EXPERT_HIDDEN, HIDDEN),), "bf16", "spectrum", 1),
-}
+WORKLOADS = {w.name: w for w in (
+    Workload(1, "tiny_f32_8x64x256", (Group(8, 64, 256),), "f32", "normal", 3),
+    Workload(2, "one_expert_w1w3w2", (Group(2, HIDDEN, EXPERT_HIDDEN), Group(1, EXPERT_HIDDEN, HIDDEN)),
+             "bf16", "lognormal_rows", 3),
+    Workload(3, "rank_expert_batch_96", (Group(64, HIDDEN, EXPERT_HIDDEN), Group(32, EXPERT_HIDDEN, HIDDEN)),
+             "bf16", "lognormal_rows", 1),
+    Workload(4, "dense_projections", (Group(8, HIDDEN, HIDDEN), Group(4, HIDDEN, 1024)), "bf16", "normal", 1),
+    Workload(5, "conditioning_stress_128", (Group(128, EXPERT_HIDDEN, HIDDEN),), "bf16", "spectrum", 1),
+)}
 
 TINY_SVD_GROUP = Group(4, 16, 48)
 
 
-def seed_for(config: int, step: int = 0, group: int = 0, kind: int = 0) -> int:
-    return 1234 + 1000 * config + 100000 * step + 10 * group + kind
+def seed_for(index: int, step: int = 0, group: int = 0, kind: int = 0) -> int:
+    return 1234 + 1000 * index + 100000 * step + 10 * group + kind
 
 
 def _gen(device, seed: int) -> torch.Generator:
