@@ -226,9 +226,9 @@ def run_gpu(args):
                      device=dev) if fused else None
     stream = torch.cuda.current_stream(dev)
 
-    def fused_group(p, g, m):
+    def fused_group(p, g, m, param_free=None):
         mk.muon_step_batched(p, g, m, mu=MU, nesterov=True, steps=5, coeffs=QUINTIC, eps=EPS, lr=LR,
-                             weight_decay=WD, scale=0.0, workspace=ws, stream=stream)
+                             weight_decay=WD, scale=0.0, workspace=ws, stream=stream, param_free=param_free)
 
     def step(k):
         if fused:
@@ -289,8 +289,8 @@ def run_gpu(args):
             # step k's gradients arrive in device buffer k % 2, copied in group
             # by group while step k-1 computes (group j's call waits only for
             # its own gradients); group j's parameters are copied out while the
-            # next group computes, and step k+1's call for group j (which
-            # writes its parameters) waits for that copy
+            # next group computes, and in step k+1's call for group j only the
+            # launch that writes the parameters waits for that copy
             ev_in, ev_used, ev_out = [None, None], [None, None], [None] * len(groups)
 
             def copy_in(k):
@@ -313,9 +313,7 @@ def run_gpu(args):
                     copy_in(k + 1)
                 for j, (p, g, m) in enumerate(zip(p_views, g_views[i], m_views)):
                     stream.wait_event(ev_in[i][j])
-                    if ev_out[j] is not None:
-                        stream.wait_event(ev_out[j])
-                    fused_group(p, g, m)
+                    fused_group(p, g, m, param_free=ev_out[j])
                     s_out.wait_event(stream.record_event())
                     with torch.cuda.stream(s_out):
                         host_p_views[j].copy_(p, non_blocking=True)

@@ -42,6 +42,8 @@ extern "C" {
 struct CUstream_st;
 /* A cudaStream_t of the caller (same object); NULL is the legacy default stream. */
 typedef struct CUstream_st *muon_stream_t;
+/* A CUDA event (cudaEvent_t / CUevent), passed through unchanged. */
+typedef struct CUevent_st *muon_event_t;
 
 typedef enum {
   MUON_OK = 0,
@@ -208,6 +210,22 @@ int muon_step_batched_schedule(void *param, const void *grad, float *momentum, i
                                int64_t cols, float mu, int nesterov, int steps, const float *coeffs, float eps,
                                float lr, float weight_decay, float scale, void *workspace, size_t workspace_bytes,
                                muon_stream_t stream);
+
+/* muon_step_batched whose one parameter-writing launch waits for an event.
+ * Of the step's launches only the last (the final Newton-Schulz iteration
+ * with the update, or the update alone when steps == 0) writes `param`; it is
+ * ordered after `param_free` on `stream` (cudaStreamWaitEvent).  The momentum
+ * and the earlier iterations are not, so work on other streams that still
+ * reads the previous parameters (a copy to host memory, say) overlaps them.
+ * param_free is an event the caller has recorded, or NULL (then this is
+ * muon_step_batched).  Results are bit for bit those of muon_step_batched.
+ * Errors as muon_step_batched, and MUON_ERR_CUDA if the wait cannot be
+ * enqueued.
+ */
+int muon_step_batched_after(void *param, const void *grad, float *momentum, int64_t batch, int64_t rows,
+                            int64_t cols, float mu, int nesterov, int steps, const float coeffs[3], float eps,
+                            float lr, float weight_decay, float scale, void *workspace, size_t workspace_bytes,
+                            muon_event_t param_free, muon_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * The whole Muon step on matrices that live in host memory (FlexShard

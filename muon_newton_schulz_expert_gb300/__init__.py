@@ -64,6 +64,8 @@ SIGNATURES = {
     "muon_step_batched": (_INT, [_P, _P, _P, _I64, _I64, _I64, _F, _INT, _INT, _P, _F, _F, _F, _F, _P, _SIZE, _P]),
     "muon_step_batched_schedule": (_INT, [_P, _P, _P, _I64, _I64, _I64, _F, _INT, _INT, _P, _F, _F, _F, _F, _P, _SIZE,
                                           _P]),
+    "muon_step_batched_after": (_INT, [_P, _P, _P, _I64, _I64, _I64, _F, _INT, _INT, _P, _F, _F, _F, _F, _P, _SIZE,
+                                       _P, _P]),
     "muon_step_host": (_INT, [_P, _P, _P, _I64, _I64, _I64, _F, _INT, _INT, _P, _F, _F, _F, _F, _I64, _P]),
     "muon_adamw_update": (_INT, [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P]),
     "muon_adamw_update_f32": (_INT, [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P]),
@@ -308,14 +310,15 @@ def muon_step_workspace_bytes(batch, rows, cols):
 
 
 def muon_step_batched(param, grad, momentum, *, mu=0.95, nesterov=True, steps=5, coeffs=QUINTIC, eps=1e-7, lr=0.02,
-                      weight_decay=0.1, scale=0.0, workspace=None, stream=None):
+                      weight_decay=0.1, scale=0.0, workspace=None, stream=None, param_free=None):
     """The fused Muon step on one group of same-shape device matrices (in place).
 
     param and grad bf16 (batch, rows, cols), momentum fp32 of the same shape.
     Bit for bit the result of momentum -> Newton-Schulz -> update.  With
     ``workspace`` (CUDA uint8, at least ``muon_step_workspace_bytes``) no
     device memory is allocated; without it the library allocates it
-    stream-ordered.
+    stream-ordered.  With ``param_free`` (a recorded torch.cuda.Event) only
+    the launch that writes param waits for it (muon_step_batched_after).
     """
     import torch
     _need(param, torch.bfloat16, "param")
@@ -328,10 +331,15 @@ def muon_step_batched(param, grad, momentum, *, mu=0.95, nesterov=True, steps=5,
     if workspace is not None:
         _need(workspace, torch.uint8, "workspace")
         ws, ws_bytes = _ptr(workspace), workspace.numel()
-    _check("muon_step_batched", lib().muon_step_batched(
-        _ptr(param), _ptr(grad), _ptr(momentum), b, r, c, float(mu), int(bool(nesterov)), int(steps),
-        _coeffs(coeffs), float(eps), float(lr), float(weight_decay), float(scale), ws, ws_bytes,
-        _stream_handle(stream)))
+    args = (_ptr(param), _ptr(grad), _ptr(momentum), b, r, c, float(mu), int(bool(nesterov)), int(steps),
+            _coeffs(coeffs), float(eps), float(lr), float(weight_decay), float(scale), ws, ws_bytes)
+    if param_free is None:
+        _check("muon_step_batched", lib().muon_step_batched(*args, _stream_handle(stream)))
+    else:
+        if not param_free.cuda_event:
+            raise ValueError("param_free must be a recorded torch.cuda.Event")
+        _check("muon_step_batched_after", lib().muon_step_batched_after(*args, ctypes.c_void_p(param_free.cuda_event),
+                                                                        _stream_handle(stream)))
 
 
 def muon_step_batched_schedule(param, grad, momentum, coeff_rows, *, mu=0.95, nesterov=True, eps=1e-7, lr=0.02,

@@ -427,12 +427,22 @@ size_t muon_step_workspace_bytes(int64_t batch, int64_t rows, int64_t cols) {
   return muon_ns_workspace_bytes(batch, rows, cols);
 }
 
+// Orders the launch that writes W after `w_free` (if any) on stream s.
+static int wait_param_free(cudaEvent_t w_free, cudaStream_t s) {
+  if (w_free && cudaStreamWaitEvent(s, w_free, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return MUON_ERR_CUDA;
+  }
+  return MUON_OK;
+}
+
 // momentum+norm -> iterations 1..steps-1 -> last iteration with the update.
 // u lives in the second X buffer, which the rotation first writes in
-// iteration 2, after iteration 1 has read u for the last time.
+// iteration 2, after iteration 1 has read u for the last time.  Only the last
+// launch writes W; it waits for w_free first.
 static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, const Workspace &w, int64_t batch,
                       int64_t rows, int64_t cols, float mu, int nesterov, int steps, const float *cf0,
-                      int cf_stride, float eps, float kw, float ko, cudaStream_t s) {
+                      int cf_stride, float eps, float kw, float ko, cudaEvent_t w_free, cudaStream_t s) {
   const int64_t mm = std::min(rows, cols), nn = std::max(rows, cols), per = rows * cols;
   const bool transposed = rows > cols;
   auto *x1 = static_cast<__nv_bfloat16 *>(w.x1);
@@ -443,6 +453,7 @@ static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, cons
   MUON_TRY(launch_momentum_norm_bf16(G, mom, x2, batch, per, mu, nesterov, eps, w.partial, w.inv, w.inv2, s));
   if (steps == 0) {
     MUON_TRY(launch_scale_bf16(x2, x2, batch, per, w.inv, s));
+    MUON_TRY(wait_param_free(w_free, s));
     return launch_apply_bf16(W, x2, batch * per, kw, ko, s);
   }
   __nv_bfloat16 *src = x2;
@@ -452,8 +463,10 @@ static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, cons
     MUON_TRY(ns_poly(A, B, batch, mm, cf[1], cf[2], s));
     const __nv_bfloat16 *src_lo = it == 0 ? nullptr : lo;
     const float *s1 = it == 0 ? w.inv : nullptr;
-    if (it == steps - 1)
+    if (it == steps - 1) {
+      MUON_TRY(wait_param_free(w_free, s));
       return ns_axpy_apply(B, src, src_lo, W, batch, mm, nn, cf[0], s1, kw, ko, transposed, s);
+    }
     __nv_bfloat16 *dst = src == x1 ? x2 : x1;
     MUON_TRY(ns_axpy(B, src, src_lo, dst, lo, batch, mm, nn, cf[0], s1, transposed, s));
     src = dst;
@@ -466,7 +479,7 @@ static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, cons
 static int step_fused_entry(void *param, const void *grad, float *momentum, int64_t batch, int64_t rows, int64_t cols,
                             float mu, int nesterov, int steps, const float *cf, int cf_stride, float eps, float lr,
                             float weight_decay, float scale, void *workspace, size_t workspace_bytes,
-                            cudaStream_t s) {
+                            cudaEvent_t w_free, cudaStream_t s) {
   if (!isfinite(mu) || !isfinite(lr) || !isfinite(weight_decay) || !isfinite(scale)) return MUON_ERR_INVALID_ARG;
   if (batch == 0) return MUON_OK;
   if (!grad || !momentum) return MUON_ERR_INVALID_ARG;
@@ -486,7 +499,7 @@ static int step_fused_entry(void *param, const void *grad, float *momentum, int6
   }
   int st = step_fused(static_cast<__nv_bfloat16 *>(param), static_cast<const __nv_bfloat16 *>(grad), momentum,
                       carve(ws, batch, mm, nn, 2), batch, rows, cols, mu, nesterov ? 1 : 0, steps, cf, cf_stride, eps,
-                      kw, ko, s);
+                      kw, ko, w_free, s);
   if (!workspace && cudaFreeAsync(ws, s) != cudaSuccess && st == MUON_OK) st = MUON_ERR_CUDA;
   return st;
 }
@@ -498,7 +511,18 @@ int muon_step_batched(void *param, const void *grad, float *momentum, int64_t ba
   MUON_TRY(check_ns_args(param, batch, rows, cols, steps, coeffs, eps));
   const float cf[3] = {coeffs[0], coeffs[1], coeffs[2]};
   return step_fused_entry(param, grad, momentum, batch, rows, cols, mu, nesterov, steps, cf, 0, eps, lr, weight_decay,
-                          scale, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+                          scale, workspace, workspace_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int muon_step_batched_after(void *param, const void *grad, float *momentum, int64_t batch, int64_t rows,
+                            int64_t cols, float mu, int nesterov, int steps, const float coeffs[3], float eps,
+                            float lr, float weight_decay, float scale, void *workspace, size_t workspace_bytes,
+                            muon_event_t param_free, muon_stream_t stream) {
+  MUON_TRY(check_ns_args(param, batch, rows, cols, steps, coeffs, eps));
+  const float cf[3] = {coeffs[0], coeffs[1], coeffs[2]};
+  return step_fused_entry(param, grad, momentum, batch, rows, cols, mu, nesterov, steps, cf, 0, eps, lr, weight_decay,
+                          scale, workspace, workspace_bytes, reinterpret_cast<cudaEvent_t>(param_free),
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 int muon_step_batched_schedule(void *param, const void *grad, float *momentum, int64_t batch, int64_t rows,
@@ -508,7 +532,8 @@ int muon_step_batched_schedule(void *param, const void *grad, float *momentum, i
   MUON_TRY(check_ns_args(param, batch, rows, cols, steps, coeffs, eps, 3 * (int64_t)steps));
   std::vector<float> cf(coeffs, coeffs + 3 * (size_t)steps);
   return step_fused_entry(param, grad, momentum, batch, rows, cols, mu, nesterov, steps, cf.data(), 3, eps, lr,
-                          weight_decay, scale, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+                          weight_decay, scale, workspace, workspace_bytes, nullptr,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 static int adamw_consts(float lr, float beta1, float beta2, float eps, float wd, int64_t step, AdamWConsts *k) {

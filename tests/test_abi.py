@@ -161,6 +161,18 @@ def test_newer_entry_points_reject_bad_arguments_on_the_host(lib):
                                           None) == -2
     assert lib.muon_step_batched_schedule(P, P, P, 1, 8, 8, 0.95, 1, 2, sched2, 1e-7, 0.02, 0.1, 0.0, P, 64,
                                           None) == -4
+    # the same checks, before any CUDA call, with a parameter-free event (any handle; it is not touched)
+    E = ctypes.c_void_p(512)
+    assert lib.muon_step_batched_after(None, None, None, 0, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, None, 0,
+                                       E, None) == 0
+    assert lib.muon_step_batched_after(P, None, P, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, None, 0,
+                                       E, None) == -1
+    assert lib.muon_step_batched_after(P, P, P, 1, 8, 12, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, None, 0,
+                                       E, None) == -2
+    assert lib.muon_step_batched_after(P, P, P, 1, 8, 8, 0.95, 1, 5, None, 1e-7, 0.02, 0.1, 0.0, None, 0,
+                                       E, None) == -1
+    assert lib.muon_step_batched_after(P, P, P, 1, 8, 8, 0.95, 1, 5, c3, 1e-7, 0.02, 0.1, 0.0, P, 64,
+                                       E, None) == -4
     assert lib.muon_step_workspace_bytes(96, 6144, 1792) == lib.muon_ns_workspace_bytes(96, 1792, 6144)
     assert lib.muon_step_workspace_bytes(0, 8, 8) == 0
 

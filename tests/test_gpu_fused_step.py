@@ -152,3 +152,27 @@ def test_fused_step_launches_its_own_kernels(mk):
     assert trace["momentum_norm_bf16"][0] == 1
     assert trace["ns_axpy_tc"][0] == 2 and trace["ns_axpy_apply_tc"][0] == 1
     assert "norm_partial" not in trace and "apply_bf16" not in trace and "momentum_bf16" not in trace
+
+
+def test_param_free_event_orders_only_the_update(mk):
+    # a side stream sleeps, then copies the parameters and records param_free;
+    # the step's parameter-writing launch must come after that copy (which
+    # therefore sees the old parameters), and the result is unchanged
+    g, W, buf = _inputs(3, 512, 1536, 995)
+    W0 = W.clone()
+    W1, b1 = W.clone(), buf.clone()
+    mk.muon_step_batched(W1, g, b1)
+    side, snap = torch.cuda.Stream(), torch.empty_like(W)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(20_000_000)   # ~10 ms, bounded
+        snap.copy_(W)
+        ev = side.record_event()
+    mk.muon_step_batched(W, g, buf, param_free=ev)
+    torch.cuda.synchronize()
+    assert mk.muon_get_device_status() == 0
+    assert torch.equal(snap.view(torch.int16), W0.view(torch.int16))
+    assert np.array_equal(bits16(W), bits16(W1))
+    assert np.array_equal(bits32(buf), bits32(b1))
+    with pytest.raises(ValueError):
+        mk.muon_step_batched(W, g, buf, param_free=torch.cuda.Event())   # never recorded
