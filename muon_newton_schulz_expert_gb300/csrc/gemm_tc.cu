@@ -61,7 +61,10 @@ constexpr int UMMA_K = 16;
 //    a 128-row half of B) behind one full/empty barrier pair.  Each handoff
 //    (MMA commit -> producer refill -> TMA completion -> MMA issue) has a
 //    fixed cost, so two k-blocks per stage (8 MMAs per handoff) run the
-//    mainloop 4-9% faster than one where three such stages fit.
+//    mainloop 4-9% faster than one where three such stages fit.  X X^T,
+//    whose ring waits poll (below), is the exception: with polling the
+//    handoff is cheap enough that six single stages (more latency cover in
+//    the same 192 KB) win by 1%.
 //  - A stage completes only when its slowest sector arrives, so the ring must
 //    hold ~160-192 KB in flight to ride out L2/DRAM latency.
 //  - Epilogue slots: one slot = two or three 2 KB boxes per epilogue warp.
@@ -82,7 +85,7 @@ constexpr int UMMA_K = 16;
 #define MUON_AXPY_INPLACE 1
 #endif
 #ifndef MUON_KSUB_SYRK
-#define MUON_KSUB_SYRK 2
+#define MUON_KSUB_SYRK 1
 #endif
 #ifndef MUON_KSUB_POLY
 #define MUON_KSUB_POLY 2
@@ -94,7 +97,7 @@ constexpr int UMMA_K = 16;
 #define MUON_KSUB_APPLY 2
 #endif
 #ifndef MUON_STAGES_SYRK
-#define MUON_STAGES_SYRK 3
+#define MUON_STAGES_SYRK 6
 #endif
 #ifndef MUON_SLOTS_SYRK
 #define MUON_SLOTS_SYRK 1
@@ -170,10 +173,11 @@ struct Layout {
                                                 : MUON_KSUB_SYRK;
   static constexpr int stage_bytes = ksub * STAGE_BYTES;
   // The producer's and the MMA issuer's ring waits poll (wait_polled) in
-  // aX + BX and bA + cAA: measured 2% and 1% faster.  X X^T gains nothing,
-  // and the update-fused kernel loses 3% (its heavier epilogue warps share
-  // schedulers with the spinning threads), so those two suspend in try_wait.
-  static constexpr bool poll_ring = EPI == EPI_AXPY || EPI == EPI_POLY;
+  // aX + BX, bA + cAA and X X^T: measured 2%, 1% and 2.5% (X X^T with six
+  // single stages) faster.  The update-fused kernel loses 3% (its heavier
+  // epilogue warps share schedulers with the spinning threads), so it
+  // suspends in try_wait.
+  static constexpr bool poll_ring = EPI != EPI_APPLY;
   static constexpr int smem_bytes = stages * stage_bytes + epi_bytes + 1024 + num_bars * 8 + 16;
   static_assert((128 / cw) % slots == 0, "chunks per tile must fill the staging slots evenly");
   static_assert(smem_bytes <= 232448, "shared memory per CTA");
