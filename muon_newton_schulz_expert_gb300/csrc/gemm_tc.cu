@@ -61,22 +61,22 @@ constexpr int UMMA_K = 16;
 //    a 128-row half of B) behind one full/empty barrier pair.  Each handoff
 //    (MMA commit -> producer refill -> TMA completion -> MMA issue) has a
 //    fixed cost, so two k-blocks per stage (8 MMAs per handoff) run the
-//    mainloop 4-9% faster than one where three such stages fit.  X X^T,
-//    whose ring waits poll (below), is the exception: with polling the
-//    handoff is cheap enough that six single stages (more latency cover in
-//    the same 192 KB) win by 1%.
+//    mainloop 4-9% faster than one where three such stages fit.  With the
+//    ring waits polled (wait_polled) the handoff is cheap enough that X X^T
+//    and the update-fused aX + BX run single stages, with more latency cover
+//    in the same bytes: six in X X^T (1% faster), five beside the update
+//    epilogue's 48 KB of slots (3.5% faster).
 //  - A stage completes only when its slowest sector arrives, so the ring must
 //    hold ~160-192 KB in flight to ride out L2/DRAM latency.
 //  - Epilogue slots: one slot = two or three 2 KB boxes per epilogue warp.
 //    X X^T: one slot (output staging).  bA + cAA: one slot (b*A in, result
 //    over it).  aX + BX: one slot of X's halves, the result written over it,
-//    so 3 double stages fit.  aX + BX with the update: three input boxes of
-//    16-column chunks (1 KB each), W' written over them, so that 3 double
-//    stages fit there too.
-// aX + BX with the update: 16-column epilogue chunks (1 KB boxes) with W'
-// written over the slot, so that three two-k-block stages fit beside it
-#ifndef MUON_APPLY_CW16
-#define MUON_APPLY_CW16 1
+//    so 3 double stages fit.  aX + BX with the update: one slot of three
+//    2 KB boxes (X hi, X lo, W), W' written over them.
+// aX + BX with the update: epilogue chunk width, 32 columns, or 16 (1 KB
+// boxes, so that three double stages fit beside the slot)
+#ifndef MUON_APPLY_CW
+#define MUON_APPLY_CW 32
 #endif
 #ifndef MUON_AXPY_ROW_ORDER_T
 #define MUON_AXPY_ROW_ORDER_T 1
@@ -94,7 +94,7 @@ constexpr int UMMA_K = 16;
 #define MUON_KSUB_AXPY 2
 #endif
 #ifndef MUON_KSUB_APPLY
-#define MUON_KSUB_APPLY 2
+#define MUON_KSUB_APPLY 1
 #endif
 #ifndef MUON_STAGES_SYRK
 #define MUON_STAGES_SYRK 6
@@ -115,7 +115,7 @@ constexpr int UMMA_K = 16;
 #define MUON_SLOTS_AXPY 1
 #endif
 #ifndef MUON_STAGES_APPLY
-#define MUON_STAGES_APPLY 3
+#define MUON_STAGES_APPLY 5
 #endif
 #ifndef MUON_SLOTS_APPLY
 #define MUON_SLOTS_APPLY 1
@@ -153,16 +153,14 @@ struct Layout {
   // SYRK/POLY: a slot is [direct box][mirror box], with no separate output.
   // AXPY: input [X hi][X lo], the result [X' hi][X' lo] written over it (or,
   // with MUON_AXPY_INPLACE 0, into an output box of its own); APPLY: input
-  // [X hi][X lo][W] of 16-column boxes, W' written over it (or, with
-  // MUON_APPLY_CW16 0, 32-column boxes and W' in a box of its own, so that
-  // fetching the next input never waits for the previous store to read).
+  // [X hi][X lo][W] of cw-column boxes, W' written over it.
   // epilogue chunk width in columns (boxes of 32 rows x cw)
-  static constexpr int cw = (EPI == EPI_APPLY && MUON_APPLY_CW16) ? 16 : 32;
+  static constexpr int cw = EPI == EPI_APPLY ? MUON_APPLY_CW : 32;
+  static_assert(cw == 32 || cw == 16, "epilogue chunks of 32 or 16 columns");
   static constexpr int box_bytes = 32 * cw * 2;
   static constexpr int in_bytes = (EPI == EPI_APPLY ? 3 : 2) * box_bytes;
   static_assert(EPI >= EPI_AXPY || in_bytes == EPI_BUF, "the symmetric epilogues address slots of EPI_BUF bytes");
-  static constexpr bool inplace =
-      (EPI == EPI_AXPY && MUON_AXPY_INPLACE != 0) || (EPI == EPI_APPLY && MUON_APPLY_CW16 != 0);
+  static constexpr bool inplace = (EPI == EPI_AXPY && MUON_AXPY_INPLACE != 0) || EPI == EPI_APPLY;
   static constexpr int out_bytes = inplace ? 0 : EPI == EPI_APPLY ? box_bytes : EPI == EPI_AXPY ? 2 * box_bytes : 0;
   static constexpr int epi_bytes = EPI_WARPS * (slots * in_bytes + out_bytes);
   static constexpr int num_bars = 2 * stages + 5 + EPI_WARPS * slots;
@@ -172,12 +170,6 @@ struct Layout {
                               : EPI == EPI_POLY ? MUON_KSUB_POLY
                                                 : MUON_KSUB_SYRK;
   static constexpr int stage_bytes = ksub * STAGE_BYTES;
-  // The producer's and the MMA issuer's ring waits poll (wait_polled) in
-  // aX + BX, bA + cAA and X X^T: measured 2%, 1% and 2.5% (X X^T with six
-  // single stages) faster.  The update-fused kernel loses 3% (its heavier
-  // epilogue warps share schedulers with the spinning threads), so it
-  // suspends in try_wait.
-  static constexpr bool poll_ring = EPI != EPI_APPLY;
   static constexpr int smem_bytes = stages * stage_bytes + epi_bytes + 1024 + num_bars * 8 + 16;
   static_assert((128 / cw) % slots == 0, "chunks per tile must fill the staging slots evenly");
   static_assert(smem_bytes <= 232448, "shared memory per CTA");
@@ -279,6 +271,9 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Watch w
 // The same bounded wait by polling with test_wait: the thread is never
 // suspended, so it sees the phase flip without a wake-up delay, at the price
 // of the issue slots its spinning takes from warps on the same scheduler.
+// The producer and the MMA issuer wait on the operand ring this way: measured
+// 1-2.5% faster per kernel than suspending in try_wait (and it lets the
+// update-fused kernel and X X^T profit from single-k-block stages).
 __device__ __forceinline__ bool wait_polled(uint32_t bar, uint32_t parity, Watch w) {
   if (mbar_test_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
@@ -545,8 +540,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int kb0 = EPI >= EPI_AXPY ? (int)((long long)((ti + tj) % kt) * num_kb / kt) : 0;
         bool ok = true;
         for (int i = 0; i < num_steps; ++i) {
-          if (!(Layout<EPI>::poll_ring ? wait_polled(EMPTY(stage), phase ^ 1u, w)
-                                       : wait_bounded(EMPTY(stage), phase ^ 1u, w))) {
+          if (!wait_polled(EMPTY(stage), phase ^ 1u, w)) {
             ok = false;
             break;
           }
@@ -601,7 +595,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t d = tmem + (uint32_t)(acc * ACC_COLS);
         bool ok = true;
         for (int i = 0; i < num_steps; ++i) {  // i-th stage of the tile in the producer's order
-          if (!(Layout<EPI>::poll_ring ? wait_polled(FULL(stage), phase, w) : wait_bounded(FULL(stage), phase, w))) {
+          if (!wait_polled(FULL(stage), phase, w)) {
             ok = false;
             break;
           }
@@ -649,8 +643,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // boxes of chunk g + SLOTS are fetched into the slot once that store has
     // read it.  APPLY also stages the box of W and writes W' = bf16(kw W +
     // ko hi'), the parameter update of the unfused path, operation for
-    // operation, over the slot, in chunks of 16 columns (three 1 KB boxes) so
-    // that the ring keeps three double stages.  Lane i owns row i of the box,
+    // operation, over the slot, in chunks of MUON_APPLY_CW columns (three
+    // 2 KB boxes, or 1 KB ones for 16 columns).  Lane i owns row i of the box,
     // which is TMEM lane 32q + i; the swizzle spanning a box row (64 or 32
     // bytes) makes these row reads conflict-free.
     constexpr bool APPLY = EPI == EPI_APPLY;
