@@ -26,10 +26,9 @@
 // shared memory, which is what keeps its bandwidth below the tensor cores'
 // appetite.
 //   warp 0 lane 0  TMA producer (both CTAs): 128x64 bf16 boxes, 128-byte
-//                  swizzle, a ring of 3 stages of two k-blocks (Layout);
-//                  completion is
-//                  signalled on the even CTA's "full" barrier, which counts
-//                  the bytes of both halves;
+//                  swizzle, a ring of stages of one or two k-blocks
+//                  (Layout); completion is signalled on the even CTA's
+//                  "full" barrier, which counts the bytes of both halves;
 //   warp 1         TMEM allocation of 512 columns (two 128 x 256 fp32
 //                  accumulators) in both CTAs; lane 0 of the even CTA issues
 //                  the MMAs and multicasts tcgen05.commit to both CTAs;
@@ -40,7 +39,8 @@
 // main loop of tile t+1.  Every mbarrier wait is bounded: when it runs out the
 // kernel records a timeout in the device error word, raises a shared abort
 // flag so the other roles stop, lets in-flight copies land, frees its TMEM and
-// returns.  No TMA multicast is used: each CTA loads its own tiles.
+// returns.  No TMA multicast is used: each CTA loads its own tiles (a pair's
+// rate does not depend on how many pairs run, so L2 reads are not the limit).
 #include <cuda.h>
 
 #include <mutex>
