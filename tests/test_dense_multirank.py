@@ -17,7 +17,7 @@ import torch.multiprocessing as mp
 
 from muon_newton_schulz_expert_gb300 import dense
 
-SHAPES = [(10, 6), (7, 9), (16, 4), (3, 5)]   # uneven splits, a matrix with fewer rows than some worlds
+SHAPES = [(10, 6), (7, 9), (16, 4), (3, 5), (1, 4)]   # uneven splits; fewer rows than ranks (empty shards)
 MU, LR = 0.9, 0.05
 
 
@@ -95,6 +95,10 @@ def test_row_splits_and_owners():
     assert dense.row_splits(10, 3) == [(0, 4), (4, 7), (7, 10)]
     assert dense.row_splits(3, 4) == [(0, 1), (1, 2), (2, 3), (3, 3)]
     assert dense.row_splits(6144, 8)[-1] == (5376, 6144)
+    for rows in (0, 1, 5, 10, 1792):
+        for world in (1, 2, 3, 4, 7):
+            got = [b - a for a, b in dense.row_splits(rows, world)]
+            assert got == [t.shape[0] for t in torch.tensor_split(torch.empty(rows), world)], (rows, world)
     for rows in (1, 7, 10, 6144):
         for world in (1, 2, 3, 8):
             s = dense.row_splits(rows, world)
