@@ -4,9 +4,8 @@ Per 1792 x 6144 matrix and quintic iteration, with the symmetric products
 counted once per computed triangle: X X^T takes m^2 n multiply-adds' worth of
 flops (half of the dense 2 m^2 n), A A takes m^3 (half of 2 m^3), and aX + BX
 takes the dense 2 m^2 n.  Five iterations give 3.247e11 flops per matrix and
-4.52e11 dense-equivalent; the 96-matrix workload is 3.117e13 (the figures of
-the hot-path scope table).  The elementwise kernels' bytes are the bytes each
-element moves once.
+4.52e11 dense-equivalent; the 96-matrix workload is 3.117e13.  The elementwise
+kernels' bytes are the bytes each element moves once.
 """
 
 import pytest
