@@ -90,8 +90,9 @@ int muon_momentum_update_f32(const float *grad, float *momentum, float *update_o
  * Arithmetic: bf16 operands on the tensor cores with fp32 accumulation, fp32
  * epilogues, bf16 (round to nearest even) storage of A and B, and X carried
  * between the steps as two bf16 halves (hi = bf16(X), lo = bf16(X - hi)):
- * the tensor cores read hi, the a*X term uses hi + lo.  The 1/(||X||_F + eps) factor is applied inside the first
- * iteration's epilogues, not as a separate pass.
+ * the tensor cores read hi, the a*X term uses hi + lo.  The
+ * 1/(||X||_F + eps) factor is applied inside the first iteration's
+ * epilogues, not as a separate pass.
  * Requirements of the bf16 path: m and n multiples of 8 and X 16-byte
  * aligned (TMA strides), else MUON_ERR_UNSUPPORTED.
  * Workspace: muon_ns_batched allocates muon_ns_workspace_bytes() bytes
@@ -120,7 +121,7 @@ int muon_ns_batched_schedule_f32(float *X, int64_t batch, int64_t m, int64_t n, 
                                  float eps, muon_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * Newton-Schulz that allocates nothing.  The paper has no counterpart: this
+ * Newton-Schulz that allocates nothing.  Not part of the method itself: this
  * entry point exists for callers that cannot allocate device memory -- a host
  * that owns all device memory through its own arena and forbids allocations by
  * the libraries it loads, a runtime with a fixed memory budget that must not
