@@ -447,3 +447,112 @@ def test_quintic_then_cubic_reaches_polar_factor():
 def test_schedule_shape_is_checked():
     with pytest.raises(ValueError):
         O.newton_schulz(np.ones((4, 8)), 3, [O.QUINTIC] * 2)
+
+
+# --------------------------------------------------------------------------
+# the whole step: momentum -> bf16(u) -> Newton-Schulz -> update
+# --------------------------------------------------------------------------
+# Each pin below reaches the step's result through a route that does not use
+# the oracle's composition: torch's own bf16 conversion, numpy's SVD, exact
+# dyadic arithmetic.  The planted mistakes are the plausible ones of the
+# composition (FlexShard section: one fp32 state per parameter; Newton-Schulz
+# on each whole matrix; the update with its shape scale).
+def torch_bf16(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def step_pins(shape=(2, 16, 40), seed=30):
+    """Runs the pins on one stack; returns the list of pins that failed."""
+    rng = np.random.default_rng(seed)
+    bad = []
+    # fp32 gradients that are not bf16 values, so rounding u to bf16 matters
+    g = (rng.standard_normal(shape) * (1 + rng.random(shape) / 64)).astype(np.float32)
+    zero = np.zeros(shape, np.float32)
+    W0 = np.zeros(shape, np.float64)
+    # (1) mu = 0 from a zero buffer: u = g exactly, the Newton-Schulz input is
+    # bf16(g); with W = 0, lr = 1, wd = 0 and scale 1 the new parameter is -O.
+    r = O.muon_step(W0, g, zero, mu=0.0, lr=1.0, weight_decay=0.0, scale=1.0)
+    want = np.stack([closed_form(torch_bf16(g[i]), 5, O.QUINTIC, 1e-7) for i in range(shape[0])])
+    if not (rel_fro(r["O"], want) < 1e-10 and rel_fro(r["param"], -want) < 1e-10):
+        bad.append("ns_input_is_bf16_of_u")
+    # (2) lr = 0 leaves the parameters as they were
+    W = O.bf16_round((0.02 * rng.standard_normal(shape)).astype(np.float32)).astype(np.float64)
+    r = O.muon_step(W, g, zero, lr=0.0, weight_decay=0.1)
+    if not np.array_equal(r["param"], W):
+        bad.append("lr_zero_is_identity")
+    # (3) a zero gradient from a zero buffer gives O = 0: pure decoupled decay,
+    # exact on dyadic data (1 - 0.5 * 0.5 = 3/4)
+    Wd = rng.integers(-64, 64, shape).astype(np.float64) / 16
+    r = O.muon_step(Wd, zero, zero, lr=0.5, weight_decay=0.5)
+    if not (np.array_equal(r["O"], np.zeros(shape)) and np.array_equal(r["param"], 0.75 * Wd)):
+        bad.append("decay_alone")
+    # (4) two momentum steps with mu = 1/2 on dyadic gradients: u2 = g2 + (g1/2 + g2)/2
+    # exactly (fp32 and bf16 represent it), O2 = closed form of u2; decay and
+    # update combined: W' = (1 - lr wd) W - lr O with dyadic lr, wd
+    g1 = rng.integers(-8, 9, shape).astype(np.float32) / 8
+    g2 = rng.integers(-8, 9, shape).astype(np.float32) / 8
+    r1 = O.muon_step(Wd, g1, zero, mu=0.5, lr=0.25, weight_decay=0.5, scale=1.0)
+    r2 = O.muon_step(Wd, g2, r1["buf"], mu=0.5, lr=0.25, weight_decay=0.5, scale=1.0)
+    u2 = g2.astype(np.float64) + 0.5 * (0.5 * g1.astype(np.float64) + g2)
+    want2 = np.stack([closed_form(u2[i], 5, O.QUINTIC, 1e-7) for i in range(shape[0])])
+    if not (np.array_equal(r1["buf"], g1) and np.array_equal(r2["buf"], 0.5 * g1 + g2)
+            and rel_fro(r2["O"], want2) < 1e-10
+            and rel_fro(r2["param"], 0.875 * Wd - 0.25 * want2) < 1e-12):
+        bad.append("nesterov_composition")
+    return bad
+
+
+def scale_pins():
+    """The default shape scale on the stored shape, at the pages' expert shapes
+    (steps = 0: O is u / (||u|| + eps), cheap at full size)."""
+    bad = []
+    for (rows, cols), s in (((6144, 1792), math.sqrt(6144 / 1792)), ((1792, 6144), 1.0)):
+        g = workloads.gradients(1, rows, cols, 41).float().numpy()
+        r = O.muon_step(np.zeros((1, rows, cols)), g, np.zeros((1, rows, cols), np.float32), steps=0,
+                        lr=1.0, weight_decay=0.0)
+        u = g.astype(np.float64) * (1 + 0.95)          # mu = 0.95 from zero: u = g + 0.95 g
+        u = torch_bf16(u.astype(np.float32)).astype(np.float64)
+        O0 = u / (math.sqrt(float(np.sum(u * u))) + 1e-7)
+        if not rel_fro(r["param"], -s * O0) < 1e-12:
+            bad.append(f"scale_{rows}x{cols}")
+    return bad
+
+
+def test_step_composition_pins_hold():
+    assert step_pins() == []
+    assert step_pins(shape=(1, 40, 16), seed=31) == []
+
+
+@pytest.mark.slow
+def test_step_scale_pins_hold_at_expert_shapes():
+    assert scale_pins() == []
+
+
+PLANTED_STEP = {
+    # Newton-Schulz fed the fp32 u instead of bf16(u)
+    "u_not_rounded": ("bf16_round", lambda x: np.asarray(x, np.float32), "ns_input_is_bf16_of_u"),
+    # Nesterov dropped: the step orthogonalises the buffer
+    "buffer_not_u": ("momentum_update",
+                     lambda g, b, mu, nesterov=True: (lambda nb: (nb, nb.copy()))(
+                         np.add(np.multiply(np.float32(mu), np.asarray(b, np.float32), dtype=np.float32),
+                                np.asarray(g, np.float32), dtype=np.float32)),
+                     "nesterov_composition"),
+    # decay applied to the update instead of the parameter
+    "decay_on_update": ("apply_update",
+                        lambda W, Ob, lr, wd, s: np.asarray(W, np.float64) - lr * s * (1 - lr * wd) * np.asarray(Ob),
+                        "decay_alone"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PLANTED_STEP))
+def test_planted_step_mistakes_are_caught(monkeypatch, name):
+    attr, bad_fn, pin = PLANTED_STEP[name]
+    monkeypatch.setattr(O, attr, bad_fn)
+    assert pin in step_pins()
+
+
+@pytest.mark.slow
+def test_planted_canonical_shape_scale_is_caught(monkeypatch):
+    # the scale taken on the m <= n orientation instead of the stored shape
+    monkeypatch.setattr(O, "default_scale", lambda r, c: math.sqrt(max(1.0, min(r, c) / max(r, c))))
+    assert "scale_6144x1792" in scale_pins()
