@@ -89,25 +89,57 @@ def aggregate_value(matrices_per_rank, world, ms_per_step_max):
     return matrices_per_rank * world / (ms_per_step_max / 1e3)
 
 
-def axpy_traffic_per_matrix():
-    """DRAM bytes per matrix of ns_axpy_tc from the committed ncu summary, or None
-    when the kernel source changed after the counters were taken."""
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ns_axpy_traffic.json")
+KERNEL_SOURCE = os.path.join(ROOT, "muon_newton_schulz_expert_gb300", "csrc", "gemm_tc.cu")
+
+
+def source_sha256():
     import hashlib
-    prof = os.path.join(ROOT, "profiles", "ns_gemm_kernels_profile8.md")
-    src = os.path.join(ROOT, "muon_newton_schulz_expert_gb300", "csrc", "gemm_tc.cu")
-    if not (os.path.exists(prof) and os.path.exists(src)):
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def axpy_traffic_per_matrix():
+    """DRAM bytes per matrix of ns_axpy_tc from the committed capture record
+    (written by --ingest-ncu), or None when the kernel source changed after
+    the counters were taken."""
+    if not os.path.exists(TRAFFIC_FILE):
         return None
-    fields = {}
-    with open(prof) as f:
-        for line in f:
-            if ":" in line and line.split(":")[0] in ("traffic_bytes_per_matrix", "source_sha256"):
-                k, v = line.split(":", 1)
-                fields[k] = v.strip()
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
-    if fields.get("source_sha256") != sha or "traffic_bytes_per_matrix" not in fields:
+    with open(TRAFFIC_FILE) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256") != source_sha256():
         return None
-    return int(fields["traffic_bytes_per_matrix"])
+    return int(rec["traffic_bytes_per_matrix"])
+
+
+def ingest_ncu(csv_path, matrices, command):
+    """Writes profiles/ns_axpy_traffic.json from an ncu raw-page CSV
+    (ncu -i <rep> --page raw --csv) of ns_gemm_kernel<2,...> (aX + BX) launches
+    that each processed `matrices` matrices."""
+    import csv
+    with open(csv_path, newline="") as f:
+        rows = list(csv.reader(f))
+    head = rows[0]
+    name_col = head.index("Kernel Name")
+    rd, wr = head.index("dram__bytes_read.sum"), head.index("dram__bytes_write.sum")
+    units = rows[1]
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+
+    def val(row, col):
+        return float(row[col].replace(",", "")) * scale.get(units[col], 1)
+
+    launches = [r for r in rows[2:] if len(r) > wr and "ns_gemm_kernel<2" in r[name_col]]
+    if not launches:
+        raise SystemExit("no ns_gemm_kernel<2,...> (aX + BX) launch in " + csv_path)
+    per_launch = [val(r, rd) + val(r, wr) for r in launches]
+    rec = {"kernel": "ns_axpy_tc (ns_gemm_kernel<2,...>)", "launches": len(launches), "matrices_per_launch": matrices,
+           "dram_bytes_per_launch": [int(x) for x in per_launch],
+           "traffic_bytes_per_matrix": int(sum(per_launch) / len(per_launch) / matrices),
+           "source": os.path.relpath(KERNEL_SOURCE, ROOT), "source_sha256": source_sha256(), "command": command}
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    print(json.dumps(rec))
 
 
 def load_peaks():
@@ -369,6 +401,7 @@ def run_gpu(args):
                                                                           max(3, args.steps // 3))
     peaks, peak_src = load_peaks()
     adamw = None if args.no_adamw else bench_adamw(mk, torch, dev, stream, float(peaks.get("hbm_gbs", 6800.0)))
+    dense_ovl = None if (args.no_dense or world > 1) else bench_dense_overlap(mk, torch, dev, stream, step)
     kernels = {}
     for name, (n, t) in sorted(trace.items()):
         ent = {"launches": n, "avg_ms": round(t / n, 4), "share": None}
@@ -395,7 +428,8 @@ def run_gpu(args):
         traffic = axpy_traffic_per_matrix() * total / len(groups)   # bytes per average launch
     roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
-            "traffic_note": "ncu dram read+write bytes per matrix (8-matrix capture) x matrices per launch",
+            "traffic_note": "ncu dram read+write bytes per matrix (profiles/ns_axpy_traffic.json, 8-matrix "
+                            "capture) x matrices per launch; null when the kernel source changed since",
             "peak_source": f"bf16_tflops_sustained ({peak_src})",
             "avg_launch_ms": round(dt / dn, 4), "launches": dn}
     tc_ms = sum(trace.get(k, (0, 0.0))[1] for k in KERNEL_FLOPS) / args.steps
@@ -416,7 +450,7 @@ def run_gpu(args):
         "tensor_kernels_tflops": round(total * FLOPS_NS / (tc_ms / 1e3) / 1e12, 1) if tc_ms else None,
         "flops_per_matrix": {"algorithmic_symmetric": FLOPS_NS, "dense_equivalent": FLOPS_NS_DENSE},
         "roofline": roof, "kernels": kernels, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
-        "adamw": adamw, "host_resident": host_res,
+        "adamw": adamw, "host_resident": host_res, "dense_overlap": dense_ovl,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -456,6 +490,63 @@ def bench_host_resident(mk, torch, dev, stream, params, grads, groups, split, to
     return {"value": round(aggregate_value(total, world, ms), 3), "unit": UNIT, "ms_per_step": round(ms, 3),
             "steps": steps, "h2d_bytes_per_step": numel * 8, "d2h_bytes_per_step": numel * 6, "chunk": 8,
             "api": "muon_step_host (pinned host parameters, gradients and momentum)"}
+
+
+def bench_dense_overlap(mk, torch, dev, stream, expert_step, reps=3):
+    """The dense matrices' step beside the experts' one (section "FlexShard:
+    Muon without communication": the dense matrices' Newton-Schulz runs on
+    their owner ranks, overlapped with the experts').  The dense workload is
+    the attention-like one (8 x 6144x6144 + 4 x 6144x1024, bf16, fp32
+    momentum), sharded over one rank here, so dense_step runs no collective:
+    it stacks each shape and makes one batched Newton-Schulz call per shape.
+    Times, with CUDA events on the main stream: the experts' step alone, the
+    dense step alone, the two one after the other on one stream, and the dense
+    step on a side stream while the experts' step runs on the main one."""
+    import workloads
+    from muon_newton_schulz_expert_gb300 import dense
+
+    shapes = [(workloads.HIDDEN, workloads.HIDDEN)] * 8 + [(workloads.HIDDEN, 1024)] * 4
+    params = [workloads.parameters(1, r, c, 8800 + i, device=dev)[0] for i, (r, c) in enumerate(shapes)]
+    grads = [workloads.gradients(1, r, c, 8900 + i, device=dev, kind="normal")[0] for i, (r, c) in enumerate(shapes)]
+    moms = [torch.zeros(r, c, device=dev) for r, c in shapes]
+    side = torch.cuda.Stream(dev)
+
+    def dense_once(st):
+        dense.dense_step(params, grads, moms, shapes, lr=LR, weight_decay=WD, stream=st)
+
+    def timed(fn):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    def both_overlapped():
+        side.wait_stream(stream)
+        expert_step(0)
+        dense_once(side)
+        stream.wait_stream(side)
+
+    expert_step(0)
+    dense_once(stream)
+    torch.cuda.synchronize(dev)
+    t_e = timed(lambda: expert_step(0))
+    t_d = timed(lambda: dense_once(stream))
+    t_seq = timed(lambda: (expert_step(0), dense_once(stream)))
+    t_ovl = timed(both_overlapped)
+    if mk.muon_get_device_status() != 0:
+        raise RuntimeError("device status not OK after the dense overlap measurement")
+    del params, grads, moms
+    return {"dense_workload": "8 x 6144x6144 + 4 x 6144x1024 bf16 (dense_step, one rank: no collective)",
+            "expert_step_ms": round(t_e, 3), "dense_step_ms": round(t_d, 3), "sequential_ms": round(t_seq, 3),
+            "overlapped_ms": round(t_ovl, 3), "overlap_saving": round(1.0 - t_ovl / t_seq, 4),
+            "timing": f"best of {reps}, CUDA events on the main stream"}
 
 
 def bench_adamw(mk, torch, dev, stream, hbm_peak, steps=10, warmup=3):
@@ -576,7 +667,15 @@ def main():
                     help="fused: one muon_step_batched call per shape group; unfused: the three separate calls")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture, if current")
+    ap.add_argument("--no-dense", action="store_true", help="skip the dense-matrix overlap measurement")
+    ap.add_argument("--ingest-ncu", metavar="CSV", default=None,
+                    help="write profiles/ns_axpy_traffic.json from an ncu raw-page CSV of aX + BX launches, then exit")
+    ap.add_argument("--ingest-matrices", type=int, default=8, help="matrices per captured launch (--ingest-ncu)")
+    ap.add_argument("--ingest-command", default="", help="the capture's command line, recorded with the figures")
     args = ap.parse_args()
+    if args.ingest_ncu:
+        ingest_ncu(args.ingest_ncu, args.ingest_matrices, args.ingest_command)
+        return
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         run_reference(args)

@@ -52,7 +52,7 @@ typedef enum {
   MUON_ERR_CUDA = -3,         /* a CUDA runtime call or kernel launch failed */
   MUON_ERR_NO_MEMORY = -4,    /* workspace allocation failed or workspace too small */
   MUON_ERR_TIMEOUT = -5,      /* a device-side bounded wait ran out (kernel returned early) */
-  MUON_ERR_DEVICE = -6        /* a device-side consistency check failed */
+  MUON_ERR_DEVICE = -6        /* a device-side consistency check failed (non-finite input norm) */
 } muon_status;
 
 /* ---------------------------------------------------------------------------
@@ -87,14 +87,20 @@ int muon_momentum_update_f32(const float *grad, float *momentum, float *update_o
  *   coeffs  host pointer to 3 floats (a, b, c); the quintic is
  *           (3.4445, -4.7750, 2.0315)
  *   eps     added to the Frobenius norm, eps >= 0 (1e-7 by convention)
- * Arithmetic: bf16 operands on the tensor cores with fp32 accumulation, fp32
- * epilogues, bf16 (round to nearest even) storage of A and B, and X carried
- * between the steps as two bf16 halves (hi = bf16(X), lo = bf16(X - hi)):
- * the tensor cores read hi, the a*X term uses hi + lo.  The
- * 1/(||X||_F + eps) factor is applied inside the first iteration's
- * epilogues, not as a separate pass.
- * Requirements of the bf16 path: m and n multiples of 8 and X 16-byte
- * aligned (TMA strides), else MUON_ERR_UNSUPPORTED.
+ * Arithmetic: 16-bit operands on the tensor cores with fp32 accumulation,
+ * fp32 epilogues, 16-bit storage (round to nearest even) of A and B, and X
+ * carried between the steps as two halves (hi, and lo = bf16(X - hi)): the
+ * tensor cores read hi, the a*X term uses hi + lo.  The 16-bit format is
+ * bf16 when min(m, n) > 256; for smaller matrices it is fp16 scaled by
+ * powers of two chosen from bounds that the coefficients give on every
+ * iterate (8 times finer than bf16; the first step's B stays bf16), which
+ * keeps small matrices, whose rounding errors average over few singular
+ * directions, as accurate as large ones.  The 1/(||X||_F + eps) factor is
+ * applied inside the first iteration's epilogues, not as a separate pass.
+ * Requirements of the tensor-core path: m and n multiples of 8 and X 16-byte
+ * aligned (TMA strides), else MUON_ERR_UNSUPPORTED; for min(m, n) <= 256
+ * also coefficients under which no iterate's norm bound passes 2^54 (fp16
+ * scaled by at least 2^-40), else MUON_ERR_UNSUPPORTED before any launch.
  * Workspace: muon_ns_batched allocates muon_ns_workspace_bytes() bytes
  * stream-ordered on `stream` (cudaMallocAsync/cudaFreeAsync from the device's
  * default memory pool); MUON_ERR_NO_MEMORY if that fails.
@@ -281,8 +287,10 @@ float muon_default_scale(int64_t rows, int64_t cols);
  * Status, self-test and tracing helpers.
  */
 /* Synchronises `stream`, then returns and clears the current device's error
- * word: MUON_ERR_TIMEOUT if a bounded wait ran out, MUON_ERR_DEVICE for a
- * failed device-side check, MUON_ERR_CUDA for a CUDA error, else MUON_OK. */
+ * word: MUON_ERR_TIMEOUT if a bounded wait ran out, MUON_ERR_DEVICE if a
+ * Newton-Schulz input (or fused step's u) had a Frobenius norm that is not
+ * finite in fp32 (an Inf or NaN entry, or entries beyond ~1.8e19; its output
+ * is then zero or NaN), MUON_ERR_CUDA for a CUDA error, else MUON_OK. */
 int muon_get_device_status(muon_stream_t stream);
 
 /* Human-readable name of a muon_status value (static string). */

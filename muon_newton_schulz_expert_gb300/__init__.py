@@ -14,7 +14,6 @@ whole-expert ownership so that the step needs no communication.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -382,7 +381,8 @@ def muon_step_host(param_host, grad_host, momentum_host, *, mu=0.95, nesterov=Tr
 
 
 def muon_default_scale(rows, cols):
-    return float(lib().muon_default_scale(rows, cols))
+    """The library's default shape scale for a stored rows x cols matrix (muon.h)."""
+    return float(lib().muon_default_scale(int(rows), int(cols)))
 
 
 def muon_get_device_status(stream=None):
@@ -442,7 +442,3 @@ def muon_step(params, grads, momenta, update_bufs=None, *, mu=0.95, nesterov=Tru
         muon_ns_batched(u, steps, coeffs, eps, stream)
         muon_apply_update(p, u, lr, weight_decay, scale, stream)
 
-
-def default_scale(rows, cols):
-    """sqrt(max(1, rows/cols)) -- host-side convenience, same value as muon_default_scale."""
-    return math.sqrt(max(1.0, rows / cols))

@@ -7,6 +7,8 @@
 // on each whole matrix; whole-expert ownership, so no communication).
 #include <math.h>
 
+#include <cmath>
+
 #include <algorithm>
 #include <atomic>
 #include <mutex>
@@ -121,25 +123,32 @@ int num_sms() {
 namespace {
 
 // Workspace of one Newton-Schulz call on [batch][mm][nn] (mm <= nn), in order:
-// two X buffers, the low half of X (bf16 path only), A, B (mm x mm each), norm
-// partials, 1/(||X||+eps) and its square.
+// two X buffers, the low half of X (tensor-core path only), A, B (mm x mm
+// each), norm partials, 1/(||X||+eps) and its square.  Every region starts on
+// a 256-byte boundary and is followed by kGapBytes that no kernel writes, so
+// that a write past a region's end lands in a gap a test can inspect rather
+// than in the next region.
 struct Workspace {
   void *x1, *x2, *lo, *a, *b;
   float *partial, *inv, *inv2;
 };
 
+constexpr size_t kGapBytes = 256;
+
+inline size_t region(size_t bytes) { return align256(bytes) + kGapBytes; }
+
 size_t ws_bytes(int64_t batch, int64_t mm, int64_t nn, size_t elem) {
-  size_t xs = align256((size_t)batch * mm * nn * elem);
-  size_t as = align256((size_t)batch * mm * mm * elem);
-  size_t fl = align256((size_t)batch * norm_partials() * sizeof(float)) + 2 * align256((size_t)batch * sizeof(float));
+  const size_t xs = region((size_t)batch * mm * nn * elem);
+  const size_t as = region((size_t)batch * mm * mm * elem);
+  const size_t fl = region((size_t)batch * norm_partials() * sizeof(float)) + 2 * region((size_t)batch * sizeof(float));
   return (elem == 2 ? 3 : 2) * xs + 2 * as + fl;
 }
 
 Workspace carve(void *base, int64_t batch, int64_t mm, int64_t nn, size_t elem) {
   uint8_t *p = static_cast<uint8_t *>(base);
   Workspace w{};
-  size_t xs = align256((size_t)batch * mm * nn * elem);
-  size_t as = align256((size_t)batch * mm * mm * elem);
+  const size_t xs = region((size_t)batch * mm * nn * elem);
+  const size_t as = region((size_t)batch * mm * mm * elem);
   w.x1 = p;
   p += xs;
   w.x2 = p;
@@ -153,9 +162,9 @@ Workspace carve(void *base, int64_t batch, int64_t mm, int64_t nn, size_t elem) 
   w.b = p;
   p += as;
   w.partial = reinterpret_cast<float *>(p);
-  p += align256((size_t)batch * norm_partials() * sizeof(float));
+  p += region((size_t)batch * norm_partials() * sizeof(float));
   w.inv = reinterpret_cast<float *>(p);
-  p += align256((size_t)batch * sizeof(float));
+  p += region((size_t)batch * sizeof(float));
   w.inv2 = reinterpret_cast<float *>(p);
   return w;
 }
@@ -186,43 +195,151 @@ int copy_async(void *dst, const void *src, size_t bytes, cudaStream_t s) {
   return e == cudaSuccess ? st : MUON_ERR_CUDA;
 }
 
-// The bf16 iteration on the canonical orientation.  `src0` holds X (mm x nn per
-// matrix).  With `final_dst` set the result ends there (which may be src0
-// itself); with final_dst == nullptr it stays in whichever buffer the last
-// iteration wrote, returned through `result`.
-// cf holds (a, b, c) for step it at cf + it * cf_stride (stride 0: one triple).
-int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *final_dst, const Workspace &w, int64_t batch, int64_t mm,
-                 int64_t nn, bool transposed, int steps, const float *cf, int cf_stride, float eps, cudaStream_t s,
-                 __nv_bfloat16 **result) {
-  const int64_t per = mm * nn;
-  MUON_TRY(launch_inv_norm_bf16(src0, batch, per, eps, w.partial, w.inv, w.inv2, s));
-  auto *x1 = static_cast<__nv_bfloat16 *>(w.x1);
-  auto *x2 = static_cast<__nv_bfloat16 *>(w.x2);
-  if (steps == 0) {
-    *result = final_dst ? final_dst : src0;
-    return launch_scale_bf16(src0, *result, batch, per, w.inv, s);
+// Storage plan of the tensor-core iteration.  What an iteration produces (A,
+// B and X's high half) is stored in 16 bits, in one of two formats chosen per
+// call by the matrix size:
+//  - bf16, for m > kF16MaxRows: the computed values rounded to bf16, no
+//    scaling;
+//  - fp16 scaled by powers of two, for m <= kF16MaxRows, except the first
+//    iteration's B, which stays bf16 because it meets the bf16 input u in one
+//    tensor-core product (kind::f16 takes both operands in one format).  A
+//    value v is stored as fp16(sigma v), sigma chosen from a bound on the
+//    matrix's spectral norm, which bounds every entry: ||X_0|| <= ||X_0||_F
+//    <= 1 after the normalisation, and per step ||A|| = ||X||^2, ||B|| <=
+//    max |b l + c l^2| over l in [0, ||A||] and ||X'|| <= max |a x + b x^3 +
+//    c x^5| over x in [0, ||X||] (the iteration acts on each singular value
+//    by these scalar maps).  The largest entry is then held near 2^14 (fp16
+//    reaches 65504), and the powers of two fold exactly into the constants
+//    each epilogue already applies.
+// Why two formats: fp16 keeps 11 significant bits against bf16's 8.  With
+// bf16 storage the output's error is ~1% of its norm on large matrices, but
+// small ones have few singular directions to average the rounding over, and
+// up to m ~ 16 a third of random inputs exceed 2% (a CPU model of these
+// rounding points: tests/test_rounding_model.py); with fp16 storage every size
+// stays near the 0.2% of the final bf16 rounding.  On large batches, though,
+// fp16 products draw more power than bf16 ones, and under the board's power
+// cap that lowered the clock and the step's throughput by 3.5%.  Matrices up
+// to kF16MaxRows rows are small enough for that not to matter.
+constexpr int64_t kF16MaxRows = 256;
+
+struct IterPlan {
+  float syrk_mul;          // sigma_A / sigma_in^2
+  float poly_b, poly_c;    // b sigma_B / sigma_A, c sigma_B / sigma_A^2
+  float axpy_a, axpy_mul;  // a sigma_B, sigma_out / (sigma_in sigma_B)
+  int tin;                 // format of X and B in this iteration's product
+  int store;               // format of A, and of B and X' unless bf16 is required
+};
+
+// max |a x + b x^3 + c x^5| over x in [0, hi]: the ends and the stationary
+// points, x^2 = t a root of 5c t^2 + 3b t + a
+double max_abs_quintic(double a, double b, double c, double hi) {
+  auto f = [&](double x) { return fabs(x * (a + x * x * (b + c * x * x))); };
+  double best = f(hi);
+  double roots[2];
+  int nr = 0;
+  if (c != 0.0) {
+    const double disc = 9.0 * b * b - 20.0 * a * c;
+    if (disc >= 0.0) {
+      const double sq = sqrt(disc);
+      roots[nr++] = (-3.0 * b + sq) / (10.0 * c);
+      roots[nr++] = (-3.0 * b - sq) / (10.0 * c);
+    }
+  } else if (b != 0.0) {
+    roots[nr++] = -a / (3.0 * b);
   }
-  auto *A = static_cast<__nv_bfloat16 *>(w.a);
-  auto *B = static_cast<__nv_bfloat16 *>(w.b);
-  auto *lo = static_cast<__nv_bfloat16 *>(w.lo);
-  __nv_bfloat16 *src = src0;
+  for (int i = 0; i < nr; ++i)
+    if (roots[i] > 0.0 && roots[i] < hi * hi) best = std::max(best, f(sqrt(roots[i])));
+  return best;
+}
+
+// max |b l + c l^2| over l in [0, hi]
+double max_abs_quad(double b, double c, double hi) {
+  auto f = [&](double l) { return fabs(l * (b + c * l)); };
+  double best = f(hi);
+  if (c != 0.0) {
+    const double l = -b / (2.0 * c);
+    if (l > 0.0 && l < hi) best = std::max(best, f(l));
+  }
+  return best;
+}
+
+// exponent e of the power of two 2^e that puts `bound` (with 1% to spare)
+// at or below 2^14; false when no such e within [-40, 40] exists
+bool storage_exp(double bound, int *e) {
+  if (!(bound > 1e-30)) {  // zero (or negligible) matrix: any scale stores it
+    *e = 0;
+    return true;
+  }
+  if (!std::isfinite(bound)) return false;
+  const int k = 14 - (int)ceil(log2(bound * 1.01));
+  if (k > 40) {
+    *e = 40;
+    return true;
+  }
+  if (k < -40) return false;
+  *e = k;
+  return true;
+}
+
+int plan_ns(int64_t mm, int steps, const float *cf, int cf_stride, std::vector<IterPlan> *plan) {
+  plan->assign((size_t)steps, IterPlan{});
+  const int store = mm <= kF16MaxRows ? kF16 : kBF16;
+  double bx = 1.0;   // bound on ||X_k||
+  int ex = 0;        // sigma_X of the current input (the first input carries s instead)
   for (int it = 0; it < steps; ++it) {
+    const double a = cf[(size_t)it * cf_stride], b = cf[(size_t)it * cf_stride + 1],
+                 c = cf[(size_t)it * cf_stride + 2];
+    int ea = 0, eb = 0, eo = 0;
+    if (store == kF16) {   // bf16 shares fp32's exponent range: no scaling
+      const double ba = bx * bx, bb = max_abs_quad(b, c, ba);
+      const double bx_next = max_abs_quintic(a, b, c, bx);
+      if (!storage_exp(ba, &ea)) return MUON_ERR_UNSUPPORTED;
+      if (it > 0 && !storage_exp(bb, &eb)) return MUON_ERR_UNSUPPORTED;   // the first B is bf16
+      if (it + 1 < steps && !storage_exp(bx_next, &eo)) return MUON_ERR_UNSUPPORTED;
+      bx = bx_next;
+    }
+    const int ein = it == 0 ? 0 : ex;
+    IterPlan &q = (*plan)[it];
+    q.syrk_mul = (float)ldexp(1.0, ea - 2 * ein);
+    q.poly_b = (float)ldexp(b, eb - ea);
+    q.poly_c = (float)ldexp(c, eb - 2 * ea);
+    q.axpy_a = (float)ldexp(a, eb);
+    q.axpy_mul = (float)ldexp(1.0, eo - ein - eb);   // the last iteration stores the value itself
+    q.tin = it == 0 ? kBF16 : store;
+    q.store = store;
+    ex = eo;
+  }
+  return MUON_OK;
+}
+
+// The tensor-core iteration on the canonical orientation.  `src0` holds X
+// (bf16, mm x nn per matrix); the result (bf16) ends in `dst_final`, which may
+// be src0 itself.  Intermediate iterates live in the workspace's two X
+// buffers (fp16 high halves) and its low-half buffer.
+// cf holds (a, b, c) for step it at cf + it * cf_stride (stride 0: one triple).
+int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *dst_final, const Workspace &w, int64_t batch, int64_t mm,
+                 int64_t nn, bool transposed, int steps, const float *cf, int cf_stride, float eps, cudaStream_t s) {
+  const int64_t per = mm * nn;
+  std::vector<IterPlan> plan;
+  MUON_TRY(plan_ns(mm, steps, cf, cf_stride, &plan));
+  MUON_TRY(launch_inv_norm_bf16(src0, batch, per, eps, w.partial, w.inv, w.inv2, s));
+  if (steps == 0) return launch_scale_bf16(src0, dst_final, batch, per, w.inv, s);
+  auto *lo = static_cast<__nv_bfloat16 *>(w.lo);
+  void *src = src0;
+  for (int it = 0; it < steps; ++it) {
+    const IterPlan &q = plan[it];
     const bool last = it == steps - 1;
-    __nv_bfloat16 *dst = (src == x1) ? x2 : x1;
-    if (last && final_dst && final_dst != src) dst = final_dst;
-    const float *c = cf + (size_t)it * cf_stride;
-    MUON_TRY(ns_syrk(src, A, batch, mm, nn, it == 0 ? w.inv2 : nullptr, transposed, s));
-    MUON_TRY(ns_poly(A, B, batch, mm, c[1], c[2], s));
-    // the input X is exactly bf16 (no low half); the result leaves as bf16
-    MUON_TRY(ns_axpy(B, src, it == 0 ? nullptr : lo, dst, last ? nullptr : lo, batch, mm, nn, c[0],
-                     it == 0 ? w.inv : nullptr, transposed, s));
+    // the last iteration writes dst_final unless it would read and write the
+    // same buffer (a single step on the caller's X): then it is copied over
+    void *dst = last && src != dst_final ? static_cast<void *>(dst_final) : (src == w.x1 ? w.x2 : w.x1);
+    MUON_TRY(ns_syrk(src, q.tin, w.a, q.store, batch, mm, nn, it == 0 ? w.inv2 : nullptr, q.syrk_mul, transposed, s));
+    MUON_TRY(ns_poly(w.a, q.store, w.b, q.tin, batch, mm, q.poly_b, q.poly_c, s));
+    // the first input is exactly bf16 (no low half); the result leaves as bf16
+    MUON_TRY(ns_axpy(w.b, src, q.tin, it == 0 ? nullptr : lo, dst, last ? kBF16 : q.store, last ? nullptr : lo, batch,
+                     mm, nn, q.axpy_a, it == 0 ? w.inv : nullptr, q.axpy_mul, transposed, s));
     src = dst;
   }
-  if (final_dst && src != final_dst) {
-    MUON_TRY(copy_async(final_dst, src, (size_t)batch * per * 2, s));
-    src = final_dst;
-  }
-  *result = src;
+  if (src != dst_final) MUON_TRY(copy_async(dst_final, src, (size_t)batch * per * 2, s));
   return MUON_OK;
 }
 
@@ -264,14 +381,15 @@ int ns_bf16_entry(void *X, int64_t batch, int64_t m, int64_t n, int steps, const
                   void *workspace, size_t workspace_bytes, cudaStream_t s) {
   if (batch == 0) return MUON_OK;
   if (m % 8 || n % 8 || !aligned16(X)) return MUON_ERR_UNSUPPORTED;
+  std::vector<IterPlan> plan;
+  MUON_TRY(plan_ns(std::min(m, n), steps, cf, cf_stride, &plan));
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MUON_ERR_INVALID_ARG;
   const int64_t mm = std::min(m, n), nn = std::max(m, n);
   if (workspace_bytes < ws_bytes(batch, mm, nn, 2)) return MUON_ERR_NO_MEMORY;
   if (!device_error_word()) return MUON_ERR_CUDA;
   Workspace w = carve(workspace, batch, mm, nn, 2);
   auto *x = static_cast<__nv_bfloat16 *>(X);
-  __nv_bfloat16 *res = nullptr;
-  return ns_bf16_core(x, x, w, batch, mm, nn, m > n, steps, cf, cf_stride, eps, s, &res);
+  return ns_bf16_core(x, x, w, batch, mm, nn, m > n, steps, cf, cf_stride, eps, s);
 }
 
 // Allocates the workspace stream-ordered on s around ns_bf16_entry.
@@ -279,6 +397,8 @@ int ns_bf16_alloc(void *X, int64_t batch, int64_t m, int64_t n, int steps, const
                   cudaStream_t s) {
   if (batch == 0) return MUON_OK;
   if (m % 8 || n % 8 || !aligned16(X)) return MUON_ERR_UNSUPPORTED;
+  std::vector<IterPlan> plan;
+  MUON_TRY(plan_ns(std::min(m, n), steps, cf, cf_stride, &plan));
   const size_t bytes = ws_bytes(batch, std::min(m, n), std::max(m, n), 2);
   void *ws = nullptr;
   if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess || !ws) {
@@ -352,6 +472,19 @@ size_t muon_ns_workspace_bytes_f32(int64_t batch, int64_t m, int64_t n) {
   if (batch <= 0 || m < 1 || n < 1) return 0;
   return ws_bytes(batch, std::min(m, n), std::max(m, n), 4);
 }
+
+}  // extern "C"
+
+namespace muon {
+int ns_precheck(const void *X, int64_t batch, int64_t m, int64_t n, int steps, const float *coeffs, float eps) {
+  MUON_TRY(check_ns_args(X, batch, m, n, steps, coeffs, eps));
+  if (batch > 0 && (m % 8 || n % 8 || !aligned16(X))) return MUON_ERR_UNSUPPORTED;
+  std::vector<IterPlan> plan;
+  return plan_ns(std::min(m, n), steps, coeffs, 0, &plan);
+}
+}  // namespace muon
+
+extern "C" {
 
 int muon_ns_batched_ws(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3], float eps,
                        void *workspace, size_t workspace_bytes, muon_stream_t stream) {
@@ -445,10 +578,9 @@ static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, cons
                       int cf_stride, float eps, float kw, float ko, cudaEvent_t w_free, cudaStream_t s) {
   const int64_t mm = std::min(rows, cols), nn = std::max(rows, cols), per = rows * cols;
   const bool transposed = rows > cols;
-  auto *x1 = static_cast<__nv_bfloat16 *>(w.x1);
+  std::vector<IterPlan> plan;
+  MUON_TRY(plan_ns(mm, steps, cf0, cf_stride, &plan));
   auto *x2 = static_cast<__nv_bfloat16 *>(w.x2);
-  auto *A = static_cast<__nv_bfloat16 *>(w.a);
-  auto *B = static_cast<__nv_bfloat16 *>(w.b);
   auto *lo = static_cast<__nv_bfloat16 *>(w.lo);
   MUON_TRY(launch_momentum_norm_bf16(G, mom, x2, batch, per, mu, nesterov, eps, w.partial, w.inv, w.inv2, s));
   if (steps == 0) {
@@ -456,19 +588,20 @@ static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, cons
     MUON_TRY(wait_param_free(w_free, s));
     return launch_apply_bf16(W, x2, batch * per, kw, ko, s);
   }
-  __nv_bfloat16 *src = x2;
+  void *src = x2;
   for (int it = 0; it < steps; ++it) {
-    const float *cf = cf0 + (size_t)it * cf_stride;
-    MUON_TRY(ns_syrk(src, A, batch, mm, nn, it == 0 ? w.inv2 : nullptr, transposed, s));
-    MUON_TRY(ns_poly(A, B, batch, mm, cf[1], cf[2], s));
+    const IterPlan &q = plan[it];
+    MUON_TRY(ns_syrk(src, q.tin, w.a, q.store, batch, mm, nn, it == 0 ? w.inv2 : nullptr, q.syrk_mul, transposed, s));
+    MUON_TRY(ns_poly(w.a, q.store, w.b, q.tin, batch, mm, q.poly_b, q.poly_c, s));
     const __nv_bfloat16 *src_lo = it == 0 ? nullptr : lo;
     const float *s1 = it == 0 ? w.inv : nullptr;
     if (it == steps - 1) {
       MUON_TRY(wait_param_free(w_free, s));
-      return ns_axpy_apply(B, src, src_lo, W, batch, mm, nn, cf[0], s1, kw, ko, transposed, s);
+      return ns_axpy_apply(w.b, src, q.tin, src_lo, W, batch, mm, nn, q.axpy_a, s1, q.axpy_mul, kw, ko, transposed,
+                           s);
     }
-    __nv_bfloat16 *dst = src == x1 ? x2 : x1;
-    MUON_TRY(ns_axpy(B, src, src_lo, dst, lo, batch, mm, nn, cf[0], s1, transposed, s));
+    void *dst = src == w.x1 ? w.x2 : w.x1;
+    MUON_TRY(ns_axpy(w.b, src, q.tin, src_lo, dst, q.store, lo, batch, mm, nn, q.axpy_a, s1, q.axpy_mul, transposed, s));
     src = dst;
   }
   return MUON_OK;
@@ -485,6 +618,8 @@ static int step_fused_entry(void *param, const void *grad, float *momentum, int6
   if (!grad || !momentum) return MUON_ERR_INVALID_ARG;
   if (rows % 8 || cols % 8 || !aligned16(param) || !aligned16(grad) || !aligned16(momentum))
     return MUON_ERR_UNSUPPORTED;
+  std::vector<IterPlan> plan;
+  MUON_TRY(plan_ns(std::min(rows, cols), steps, cf, cf_stride, &plan));
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MUON_ERR_INVALID_ARG;
   const int64_t mm = std::min(rows, cols), nn = std::max(rows, cols);
   const size_t need = ws_bytes(batch, mm, nn, 2);

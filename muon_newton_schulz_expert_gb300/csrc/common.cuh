@@ -44,6 +44,10 @@ unsigned *device_error_word();
 unsigned long long wait_timeout_ns();
 int num_sms();
 
+// The argument, shape and coefficient checks of muon_ns_batched, in its order,
+// without any CUDA call: MUON_OK when the call can go ahead.
+int ns_precheck(const void *X, int64_t batch, int64_t m, int64_t n, int steps, const float *coeffs, float eps);
+
 // ---- elementwise / reduction kernels (elementwise.cu) ----
 int launch_momentum_bf16(const __nv_bfloat16 *g, float *buf, __nv_bfloat16 *u, int64_t numel, float mu,
                          int nesterov, cudaStream_t s);
@@ -85,26 +89,32 @@ int launch_scale_f32(const float *src, float *dst, int64_t batch, int64_t per, c
                      cudaStream_t s);
 
 // ---- tensor-core GEMMs of one Newton-Schulz iteration (gemm_tc.cu) ----
-// All matrices are batched, densely packed, bf16 row-major; X is m x n (m <= n),
+// 16-bit storage formats: the caller's matrices are bf16; what the iteration
+// produces is stored in bf16 or in fp16 scaled by powers of two (see plan_ns
+// in api.cu).
+enum Fmt16 : int { kBF16 = 0, kF16 = 1 };
+// All matrices are batched, densely packed, row-major; X is m x n (m <= n),
 // stored as m x n or, with `transposed`, as its transpose (n x m).
-// A = s2[b] * X X^T          (s2 == nullptr: 1), upper triangle computed, mirrored
-int ns_syrk(const __nv_bfloat16 *X, __nv_bfloat16 *A, int64_t batch, int64_t m, int64_t n, const float *s2,
+// A = tout(mul * s2[b] * X X^T)   (s2 == nullptr: 1), upper triangle computed,
+// mirrored; X of format tin (fp16 X gives fp16 A)
+int ns_syrk(const void *X, int tin, void *A, int tout, int64_t batch, int64_t m, int64_t n, const float *s2,
+            float mul, bool transposed, cudaStream_t s);
+// B = tout(b*A + c*A A)   (A of format tin, symmetric), upper triangle computed,
+// mirrored (bf16 A gives bf16 B)
+int ns_poly(const void *A, int tin, void *B, int tout, int64_t batch, int64_t m, float b, float c, cudaStream_t s);
+// Xn = tout(mul * s1[b] * (a*X + B X))   (s1 == nullptr: 1), with X = X + X_lo
+// (B and X of format tin, X_lo bf16) and the result split into Xn and
+// Xn_lo = bf16(result - Xn); X_lo and Xn_lo may be null (zero low half / not
+// wanted) and may be the same buffer (all of X, X_lo, Xn, Xn_lo in the same
+// storage orientation)
+int ns_axpy(const void *B, const void *X, int tin, const __nv_bfloat16 *X_lo, void *Xn, int tout,
+            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, float mul,
             bool transposed, cudaStream_t s);
-// B = b*A + c*A A            (A symmetric), upper triangle computed, mirrored
-int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, float b, float c,
-            cudaStream_t s);
-// Xn = s1[b] * (a*X + B X)   (s1 == nullptr: 1), with X = X + X_lo and the
-// result split into Xn = bf16(result), Xn_lo = bf16(result - Xn); X_lo and
-// Xn_lo may be null (zero low half / not wanted) and may be the same buffer
-// (all of X, X_lo, Xn, Xn_lo in the same storage orientation)
-int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *Xn,
-            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, bool transposed,
-            cudaStream_t s);
-// The last iteration with the parameter update fused in: O = bf16(s1[b] *
-// (a*X + B X)) is not stored; W = bf16(kw*W + ko*O) in place, with W stored
-// in the same orientation as X.
-int ns_axpy_apply(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *W,
-                  int64_t batch, int64_t m, int64_t n, float a, const float *s1, float kw, float ko, bool transposed,
+// The last iteration with the parameter update fused in: O = bf16(mul * s1[b]
+// * (a*X + B X)) is not stored; W = bf16(kw*W + ko*O) in place, with W (bf16)
+// stored in the same orientation as X.
+int ns_axpy_apply(const void *B, const void *X, int tin, const __nv_bfloat16 *X_lo, __nv_bfloat16 *W, int64_t batch,
+                  int64_t m, int64_t n, float a, const float *s1, float mul, float kw, float ko, bool transposed,
                   cudaStream_t s);
 int selftest_wait(unsigned long long timeout_ns, cudaStream_t s);
 

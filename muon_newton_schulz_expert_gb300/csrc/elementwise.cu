@@ -296,8 +296,12 @@ __global__ void sumsq_f32(const float *__restrict__ x, int64_t per, float *__res
 }
 
 // One warp per matrix: fixed-order sum of the partials, then 1/(sqrt + eps).
+// A sum of squares that is not finite (an Inf or NaN in the input, or
+// entries beyond ~1.8e19 whose squares overflow fp32) would make the factor
+// 0 or NaN and the update silently zero or NaN; it sets kErrDevice in the
+// error word, which muon_get_device_status reports as MUON_ERR_DEVICE.
 __global__ void inv_norm_final(const float *__restrict__ partial, int64_t batch, float eps, float *__restrict__ inv,
-                               float *__restrict__ inv2) {
+                               float *__restrict__ inv2, unsigned *__restrict__ err) {
   const int64_t b = blockIdx.x * (int64_t)(blockDim.x / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= batch) return;
@@ -306,6 +310,7 @@ __global__ void inv_norm_final(const float *__restrict__ partial, int64_t batch,
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (lane == 0) {
+    if (!isfinite(s) && err) atomicOr(err, kErrDevice);
     float r = 1.0f / (sqrtf(s) + eps);
     inv[b] = r;
     if (inv2) inv2[b] = r * r;
@@ -467,7 +472,8 @@ int launch_apply_f32(float *w, const float *o, int64_t numel, float kw, float ko
 static int launch_final(const float *partial, int64_t batch, float eps, float *inv, float *inv2, cudaStream_t s) {
   trace_before(kTraceNormFinal, s);
   const int warps = 4;
-  inv_norm_final<<<(unsigned)((batch + warps - 1) / warps), warps * 32, 0, s>>>(partial, batch, eps, inv, inv2);
+  inv_norm_final<<<(unsigned)((batch + warps - 1) / warps), warps * 32, 0, s>>>(partial, batch, eps, inv, inv2,
+                                                                                 device_error_word());
   return trace_after(kTraceNormFinal, s);
 }
 

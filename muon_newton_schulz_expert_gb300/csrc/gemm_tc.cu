@@ -9,13 +9,28 @@
 //   X' = a X + B X        (full m x n)
 // The first iteration also applies the Frobenius factor s = 1/(||X||_F+eps):
 // A gets s^2, X' gets s (so X0 = s X is never stored).
-// X is carried between iterations as a pair of bf16 halves, hi = bf16(X) and
-// lo = bf16(X - hi): the tensor cores read hi only, while the a X term of the
-// epilogue uses hi + lo.  Rounding X itself to bf16 would inject noise of
-// relative size 2^-9 into every singular direction each iteration, and the
-// quintic multiplies small singular values by up to a = 3.4445 per step, so
-// on rank-deficient or ill-conditioned inputs that noise grows to ~10% of the
-// output; with the lo half it stays near 2^-17.
+//
+// Storage formats.  The caller's X (and the first iteration's input u) is
+// bf16.  What the iteration produces is stored in 16 bits: in bf16 for
+// matrices of more than 256 rows, and for smaller ones as fp16 scaled by a
+// power of two, sigma * value, with sigma chosen on the host from a bound on
+// the matrix's spectral norm (every entry of a matrix is at most its spectral
+// norm) so that the largest possible entry sits near 2^14, well inside fp16's
+// range: A, and B and X's high half from the second iteration on (the first
+// iteration's B meets the bf16 u in one product, and tcgen05.mma of kind::f16
+// takes both operands in one format).  fp16 keeps 11 significant bits against
+// bf16's 8, so each rounding is 8x smaller; the scaling keeps fp16's narrow
+// exponent range away from overflow and moves its subnormal floor ~2^-28
+// below the largest entry.  The powers of two fold into the epilogues'
+// existing constants, exactly.
+// X is carried between iterations as a pair of halves, hi (bf16(X) or
+// fp16(sigma X)) and lo = bf16(sigma X - hi): the tensor cores read hi only,
+// while the a X term of the epilogue uses hi + lo.  Rounding X itself to 16
+// bits would inject noise into every singular direction each iteration, and
+// the quintic multiplies small singular values by up to a = 3.4445 per step,
+// so on rank-deficient or ill-conditioned inputs that noise grows to percent
+// level in the output (10% with bf16, 1-2% with fp16); with the lo half it
+// stays near 2^-17.
 //
 // Design: persistent CTA pairs (clusters of 2), one CTA per SM, 320 threads,
 // warp-specialised.  A pair computes a 256 x 256 output tile with
@@ -42,6 +57,7 @@
 // returns.  No TMA multicast is used: each CTA loads its own tiles (a pair's
 // rate does not depend on how many pairs run, so L2 reads are not the limit).
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include <mutex>
 
@@ -185,16 +201,17 @@ struct Params {
   int tiles_per_mat;
   int row_order;               // aX + BX: tiles ordered along rows (1) or down columns (0)
   long long num_tiles;
-  __nv_bfloat16 *out;
+  void *out;                   // 16-bit elements
   long long out_ld, out_mat;   // row stride and matrix stride in elements
-  const __nv_bfloat16 *src;    // epilogue operand (A for POLY, X for AXPY)
+  const void *src;             // epilogue operand (A for POLY, X for AXPY), 16-bit elements
   long long src_ld, src_mat;
   const float *scale;          // per-matrix factor (SYRK: s^2, AXPY: s) or null
+  float mul;                   // SYRK, AXPY: power-of-two storage factor, times scale[mat]
   // AXPY only: low halves of X (X = hi + lo, hi = bf16(X), lo = bf16(X - hi));
   // read at the element the thread then writes, so one buffer serves in place
   const __nv_bfloat16 *src_lo;
   __nv_bfloat16 *out_lo;
-  float a, b, c;
+  float a, b, c;               // AXPY: a; POLY: b, c (with the storage factors folded in)
   float kw, ko;                // APPLY only: W' = kw W + ko O
   unsigned *err;
   unsigned long long timeout_ns;
@@ -412,11 +429,48 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, each operand
-// K-major or MN-major (bits 15 and 16), N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+// Instruction descriptor of kind::f16: fp32 D (bit 4), A and B both bf16
+// (format 1 at bits 7 and 10) or both fp16 (format 0), each operand K-major
+// or MN-major (bits 15 and 16), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool a_mn_major, bool b_mn_major, int tin) {
+  return (1u << 4) | (tin == kBF16 ? (1u << 7) | (1u << 10) : 0u) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// Two floats to a pair of 16-bit values of format T (round to nearest even),
+// as one 32-bit word, and back.
+template <int T>
+__device__ __forceinline__ uint32_t pack2(float x, float y) {
+  if (T == kBF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    return *reinterpret_cast<uint32_t *>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(x, y);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+}
+
+template <int T>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+  if (T == kBF16) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&v);
+    return __bfloat1622float2(h);
+  } else {
+    __half2 h = *reinterpret_cast<__half2 *>(&v);
+    return __half22float2(h);
+  }
+}
+
+// One float to the 16-bit pattern of format T.
+template <int T>
+__device__ __forceinline__ uint16_t cvt16(float x) {
+  if (T == kBF16) {
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t *>(&h);
+  } else {
+    __half h = __float2half_rn(x);
+    return *reinterpret_cast<uint16_t *>(&h);
+  }
 }
 
 // Tile t -> (matrix, row tile, column tile) of 256 x 256 pair tiles.
@@ -452,10 +506,23 @@ __device__ __forceinline__ void decode_tile(const Params &p, long long t, int &m
 
 union Pack8 {
   uint4 v;
-  __nv_bfloat162 h[4];
+  uint32_t w[4];   // pairs of 16-bit values
 };
 
-template <int EPI, bool A_MN, bool B_MN>
+// Bounded wait used on the way out after an abort: waits for the phase of
+// `bar` with the given parity to complete, for at most limit_ns, without
+// looking at the abort flag (the caller has already given up).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > limit_ns) return;
+}
+
+// TIN: the 16-bit format of both tensor-core operands (which is also that of
+// the epilogue's operand, A for POLY and X's high half for AXPY / APPLY);
+// TOUT: the format the epilogue stores (SYRK, POLY, AXPY; APPLY stores bf16).
+template <int EPI, bool A_MN, bool B_MN, int TIN, int TOUT>
 __global__ void __launch_bounds__(THREADS, 1)
     ns_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ Params p) {
@@ -464,7 +531,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int STAGES = Layout<EPI>::stages;
   constexpr int KSUB = Layout<EPI>::ksub;
   constexpr int SBYTES = Layout<EPI>::stage_bytes;
-  uint8_t *epi_smem = smem + STAGES * SBYTES;  // AXPY staging slots, 1024-aligned
+  static_assert(STAGES <= 32, "the producer tracks its stages in a 32-bit mask");
+  uint8_t *epi_smem = smem + STAGES * SBYTES;  // epilogue staging slots, 1024-aligned
   uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + Layout<EPI>::epi_bytes);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Layout<EPI>::num_bars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -498,10 +566,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (EPI >= EPI_AXPY) {
-      tma_prefetch_desc(&p.tm_src);
-      tma_prefetch_desc(&p.tm_out);
-    }
+    if (EPI != EPI_SYRK) tma_prefetch_desc(&p.tm_src);
+    if (EPI >= EPI_AXPY) tma_prefetch_desc(&p.tm_out);
   }
   if (warp == 1) {  // one warp in each CTA of the pair allocates the same columns in both
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -517,12 +583,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   const Watch w{abort_flag, p.err, p.timeout_ns};
   const int num_kb = (p.K + BK - 1) / BK;
   const int num_steps = (num_kb + KSUB - 1) / KSUB;  // stages per tile
+  // a bounded wait on the way out after an abort (a fraction of the normal limit)
+  const unsigned long long drain_ns = p.timeout_ns < 20000000ull ? p.timeout_ns : 20000000ull;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer (both CTAs)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;   // stages ever filled, and the parity of their last fill
       for (long long t = cid; t < p.num_tiles; t += ncl) {
         int mat, ti, tj;
         decode_tile<EPI>(p, t, mat, ti, tj);
@@ -550,6 +619,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           // read it finished, so no load can run ahead into the next phase)
           const uint32_t full0 = map_to_rank(FULL(stage), 0);
           if (rank == 0) mbar_expect_tx(FULL(stage), 2 * valid * STAGE_BYTES);
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
 #pragma unroll
           for (int j = 0; j < KSUB; ++j) {
             if (j >= valid) break;
@@ -580,11 +651,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (!ok) break;
       }
+      // After an abort, stages may still be filling.  CTA 0's full barrier of
+      // a stage counts both CTAs' bytes of every fill CTA 0 posted, so waiting
+      // for the last fill of each stage to complete (at once when it already
+      // did) keeps both CTAs' shared memory alive until those copies land.
+      if (*abort_flag && rank == 0)
+        for (int s2 = 0; s2 < STAGES; ++s2)
+          if (issued & (1u << s2)) drain_wait(FULL(s2), (issued_parity >> s2) & 1u, drain_ns);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (CTA 0 of the pair)
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = make_idesc(CM, BN, A_MN, B_MN);
+      constexpr uint32_t idesc = make_idesc(CM, BN, A_MN, B_MN, TIN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -638,11 +716,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------------------------------------------------------- AXPY epilogue (both CTAs)
     // X' = s (a (hi + lo) + acc) through shared memory: each warp stages a
     // 32 x 32 box of hi and of lo (TMA load, zero-filled past the edges),
-    // writes hi' = bf16(X'), lo' = bf16(X' - hi') over it (each lane over
+    // writes hi' = TOUT(X'), lo' = bf16(X' - hi') over it (each lane over
     // what it has just read) and TMA-stores it (clipped at the edges); the
     // boxes of chunk g + SLOTS are fetched into the slot once that store has
     // read it.  APPLY also stages the box of W and writes W' = bf16(kw W +
-    // ko hi'), the parameter update of the unfused path, operation for
+    // ko bf16(X')), the parameter update of the unfused path, operation for
     // operation, over the slot, in chunks of MUON_APPLY_CW columns (three
     // 2 KB boxes, or 1 KB ones for 16 columns).  Lane i owns row i of the box,
     // which is TMEM lane 32q + i; the swizzle spanning a box row (64 or 32
@@ -663,6 +741,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t *obuf = ebase + SLOTS * IN_BYTES;
     const uint32_t obuf_s = ebase_s + SLOTS * IN_BYTES;
     uint32_t ephase_bits = 0;                                // parity per slot
+    uint32_t pending = 0;                                    // slots with a load not yet waited for
     const bool lo_in = p.src_lo != nullptr, lo_out = !APPLY && p.out_lo != nullptr;
     const uint32_t etx = (lo_in ? 2u : 1u) * BOXB + (APPLY ? (uint32_t)BOXB : 0u);
     auto epi_load = [&](int slot, int m_, int row0_, int col0_) {  // lane 0 only
@@ -672,6 +751,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_load_3d(dst, &p.tm_src, bar, col0_, row0_, m_);
       if (lo_in) tma_load_3d(dst + BOXB, &p.tm_src_lo, bar, col0_, row0_, m_);
       if (APPLY) tma_load_3d(dst + 2 * BOXB, &p.tm_out, bar, col0_, row0_, m_);  // W, stored over later
+      pending |= 1u << slot;
     };
     const int rbase = (int)rank * BM + q * 32;  // this warp's rows within a pair tile
     int acc = 0;
@@ -693,7 +773,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int row0 = ti * CM + rbase;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS + half * 128);
-      const float sc = p.scale ? p.scale[mat] : 1.0f;
+      const float sc = (p.scale ? p.scale[mat] : 1.0f) * p.mul;
 #pragma unroll 1
       for (int ch = 0; ch < NCH; ++ch) {
         const int slot = ch % SLOTS;   // NCH is a multiple of SLOTS
@@ -705,6 +785,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         ephase_bits ^= 1u << slot;
+        pending &= ~(1u << slot);
         uint32_t r[32];
         __syncwarp();
         if (CW == 32)
@@ -727,17 +808,18 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int k = c * 8 + 2 * e;
-            const float2 fh = __bfloat1622float2(hv.h[e]), fl = __bfloat1622float2(lv.h[e]);
+            const float2 fh = unpack2<TIN>(hv.w[e]), fl = unpack2<kBF16>(lv.w[e]);
             const float v0 = sc * fmaf(p.a, fh.x + fl.x, __uint_as_float(r[k]));
             const float v1 = sc * fmaf(p.a, fh.y + fl.y, __uint_as_float(r[k + 1]));
-            ho.h[e] = __floats2bfloat162_rn(v0, v1);
-            const float2 hh = __bfloat1622float2(ho.h[e]);
-            if (APPLY) {  // W' = kw W + ko O, each product and the sum rounded separately
-              const float2 wf = __bfloat1622float2(wv.h[e]);
-              ho.h[e] = __floats2bfloat162_rn(__fadd_rn(__fmul_rn(p.kw, wf.x), __fmul_rn(p.ko, hh.x)),
-                                              __fadd_rn(__fmul_rn(p.kw, wf.y), __fmul_rn(p.ko, hh.y)));
+            if (APPLY) {  // O = bf16(X'); W' = kw W + ko O, each product and the sum rounded separately
+              const float2 hh = unpack2<kBF16>(pack2<kBF16>(v0, v1));
+              const float2 wf = unpack2<kBF16>(wv.w[e]);
+              ho.w[e] = pack2<kBF16>(__fadd_rn(__fmul_rn(p.kw, wf.x), __fmul_rn(p.ko, hh.x)),
+                                     __fadd_rn(__fmul_rn(p.kw, wf.y), __fmul_rn(p.ko, hh.y)));
             } else {
-              lo.h[e] = __floats2bfloat162_rn(v0 - hh.x, v1 - hh.y);
+              ho.w[e] = pack2<TOUT>(v0, v1);
+              const float2 hh = unpack2<TOUT>(ho.w[e]);
+              lo.w[e] = pack2<kBF16>(v0 - hh.x, v1 - hh.y);
             }
           }
           *reinterpret_cast<uint4 *>(ob + off) = ho.v;
@@ -769,7 +851,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       ti = ti_n;
       tj = tj_n;
     }
-    if (lane == 0) bulk_wait_all();
+    if (lane == 0) {
+      bulk_wait_all();
+      // after an abort: let the loads still filling this warp's slots land
+      if (*abort_flag)
+        for (int s2 = 0; s2 < SLOTS; ++s2)
+          if (pending & (1u << s2)) drain_wait(EBAR(ew * SLOTS + s2), (ephase_bits >> s2) & 1u, drain_ns);
+    }
   } else {
     // ---------------------------------------------------------------- SYRK / POLY epilogue (both CTAs)
     // Each warp's 32 x 32 chunk (rows row0.., columns col0.., both multiples
@@ -779,12 +867,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     // [column][row] without swizzle).  Below: nothing (the mirror of another
     // chunk covers it).  On the diagonal: element stores, (r, c >= r) and the
     // mirror (c, r) for c > r.  POLY's operand b*A arrives by TMA in the box.
+    // (Reading it into registers for the whole tile before the accumulator is
+    // ready measured 5% slower.)
     constexpr int SLOTS = Layout<EPI>::slots;
     const int ew = warp - 2;
     const int q = warp & 3, half = ew >> 2;
     uint8_t *ebase = epi_smem + ew * SLOTS * EPI_BUF;   // slots of [direct box][mirror box]
     const uint32_t ebase_s = smem_u32(ebase);
     uint32_t ephase_bits = 0;
+    uint32_t pending = 0;                               // slots with a load not yet waited for
     const int rbase = (int)rank * BM + q * 32;
     auto needs_load = [&](int row0_, int col0_) {
       return EPI == EPI_POLY && col0_ + 32 > row0_ && row0_ < p.M && col0_ < p.N;
@@ -794,6 +885,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_proxy_async_smem();
       mbar_expect_tx(bar, EPI_BOX_BYTES);
       tma_load_3d(ebase_s + slot * EPI_BUF, &p.tm_src, bar, col0_, row0_, m_);
+      pending |= 1u << slot;
     };
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -818,8 +910,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int row0 = ti * CM + rbase;
       const int row = row0 + lane;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS + half * 128);
-      const float sc = p.scale ? p.scale[mat] : 1.0f;
-      __nv_bfloat16 *outm = p.out + (long long)mat * p.out_mat;
+      const float sc = (p.scale ? p.scale[mat] : 1.0f) * p.mul;
+      uint16_t *outm = static_cast<uint16_t *>(p.out) + (long long)mat * p.out_mat;
 #pragma unroll 1
       for (int ch = 0; ch < CHUNKS; ++ch) {
         const int slot = ch % SLOTS;
@@ -834,6 +926,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           ephase_bits ^= 1u << slot;
+          pending &= ~(1u << slot);
         }
         if (in_range && !below) {
           uint32_t r[32];
@@ -853,7 +946,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 v[k] = sc * a0;
                 v[k + 1] = sc * a1;
               } else {
-                const float2 f = __bfloat1622float2(av.h[e]);
+                const float2 f = unpack2<TIN>(av.w[e]);
                 v[k] = fmaf(p.c, a0, p.b * f.x);
                 v[k + 1] = fmaf(p.c, a1, p.b * f.y);
               }
@@ -866,12 +959,12 @@ __global__ void __launch_bounds__(THREADS, 1)
               const uint32_t off = (uint32_t)(lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
               Pack8 o;
 #pragma unroll
-              for (int e = 0; e < 4; ++e) o.h[e] = __floats2bfloat162_rn(v[c * 8 + 2 * e], v[c * 8 + 2 * e + 1]);
+              for (int e = 0; e < 4; ++e) o.w[e] = pack2<TOUT>(v[c * 8 + 2 * e], v[c * 8 + 2 * e + 1]);
               *reinterpret_cast<uint4 *>(ebuf + off) = o.v;
             }
-            __nv_bfloat16 *mb = reinterpret_cast<__nv_bfloat16 *>(ebuf + EPI_BOX_BYTES);
+            uint16_t *mb = reinterpret_cast<uint16_t *>(ebuf + EPI_BOX_BYTES);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) mb[k * 32 + lane] = __float2bfloat16_rn(v[k]);
+            for (int k = 0; k < 32; ++k) mb[k * 32 + lane] = cvt16<TOUT>(v[k]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -882,12 +975,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           } else {
             // on the diagonal
-            __nv_bfloat16 *orow = outm + (long long)row * p.out_ld;
+            uint16_t *orow = outm + (long long)row * p.out_ld;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
               const int c = col0 + k;
               if (row < p.M && c < p.N) {
-                const __nv_bfloat16 h = __float2bfloat16_rn(v[k]);
+                const uint16_t h = cvt16<TOUT>(v[k]);
                 if (c >= row) orow[c] = h;
                 if (c > row) outm[(long long)c * p.out_ld + row] = h;
               }
@@ -917,7 +1010,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       ti = ti_n;
       tj = tj_n;
     }
-    if (lane == 0) bulk_wait_all();
+    if (lane == 0) {
+      bulk_wait_all();
+      // after an abort: let the loads still filling this warp's slots land
+      if (*abort_flag)
+        for (int s2 = 0; s2 < SLOTS; ++s2)
+          if (pending & (1u << s2)) drain_wait(EBAR(ew * SLOTS + s2), (ephase_bits >> s2) & 1u, drain_ns);
+    }
   }
 #undef FULL
 #undef EMPTY
@@ -929,7 +1028,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   cluster_sync_all();  // no CTA frees TMEM or exits while its peer may still use them
   if (*abort_flag) {
-    // let copies already in flight land before the shared memory is released
+    // Fallback after the bounded drains above: CTA 1's operand loads signal
+    // CTA 0's barrier, which counts them only for fills CTA 0 also posted,
+    // so a fill CTA 1 issued alone is not covered there; a copy from L2 or
+    // HBM lands within microseconds, so 200 us more leaves it ample time.
     const unsigned long long t0 = global_ns();
     while (global_ns() - t0 < 200000ull) __nanosleep(1000);
   }
@@ -970,8 +1072,9 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D map over a dense [batch][rows][cols] bf16 stack; box = box_cols columns x box_rows rows x 1 matrix.
-int make_map(CUtensorMap *map, const void *base, int64_t batch, int64_t rows, int64_t cols, int box_rows,
+// 3-D map over a dense [batch][rows][cols] stack of 16-bit elements of format
+// `fmt`; box = box_cols columns x box_rows rows x 1 matrix.
+int make_map(CUtensorMap *map, const void *base, int fmt, int64_t batch, int64_t rows, int64_t cols, int box_rows,
              int box_cols = 64, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return MUON_ERR_CUDA;
@@ -979,19 +1082,21 @@ int make_map(CUtensorMap *map, const void *base, int64_t batch, int64_t rows, in
   cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(rows * cols * 2)};
   cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUtensorMapDataType dt = fmt == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MUON_OK : MUON_ERR_CUDA;
 }
 
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, int TIN, int TOUT>
 int launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int trace_kind, cudaStream_t s) {
   if (p.num_tiles == 0) return MUON_OK;
   static std::once_flag attr_once[64];
   static int max_pairs[64];
+  static cudaError_t attr_err[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MUON_ERR_CUDA;
+  auto *kernel = ns_gemm_kernel<EPI, A_MN, B_MN, TIN, TOUT>;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(THREADS, 1, 1);
   cudaLaunchAttribute attr[1];
@@ -1001,30 +1106,26 @@ int launch(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int tr
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once[dev], [&] {
-    attr_err =
-        cudaFuncSetAttribute(ns_gemm_kernel<EPI, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<EPI>::smem_bytes);
+    attr_err[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<EPI>::smem_bytes);
     // a persistent grid must fit at once: launch no more pairs than can be co-resident
     int n = 0;
     cfg.gridDim = dim3(2 * (unsigned)std::max(1, num_sms() / 2), 1, 1);
     cfg.dynamicSmemBytes = Layout<EPI>::smem_bytes;
-    if (attr_err == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&n, ns_gemm_kernel<EPI, A_MN, B_MN>, &cfg) == cudaSuccess && n > 0)
+    if (attr_err[dev] == cudaSuccess && cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n > 0)
       max_pairs[dev] = n;
     else
       max_pairs[dev] = std::max(1, num_sms() / 2);
     cudaGetLastError();
   });
-  if (attr_err != cudaSuccess) return MUON_ERR_CUDA;
+  if (attr_err[dev] != cudaSuccess) return MUON_ERR_CUDA;
   // persistent CTA pairs over the tiles
   const long long pairs = std::min<long long>(p.num_tiles, max_pairs[dev]);
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
   cfg.dynamicSmemBytes = Layout<EPI>::smem_bytes;
   cfg.stream = s;
   trace_before(trace_kind, s);
-  cudaError_t le = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<EPI, A_MN, B_MN>, ma, mb, p);
+  cudaError_t le = cudaLaunchKernelEx(&cfg, kernel, ma, mb, p);
   const int st = trace_after(trace_kind, s);
   return le == cudaSuccess ? st : MUON_ERR_CUDA;
 }
@@ -1038,6 +1139,7 @@ Params base_params(int M, int N, int K, int64_t batch) {
   p.tiles_n = (N + BN - 1) / BN;
   p.err = device_error_word();
   p.timeout_ns = wait_timeout_ns();
+  p.mul = 1.0f;
   (void)batch;
   return p;
 }
@@ -1048,23 +1150,26 @@ int triangle_tiles(int tiles_m, int tiles_n) {
   return total;
 }
 
+bool valid_fmt(int f) { return f == kBF16 || f == kF16; }
+
 }  // namespace
 
-int ns_syrk(const __nv_bfloat16 *X, __nv_bfloat16 *A, int64_t batch, int64_t m, int64_t n, const float *s2,
-            bool transposed, cudaStream_t s) {
+int ns_syrk(const void *X, int tin, void *A, int tout, int64_t batch, int64_t m, int64_t n, const float *s2,
+            float mul, bool transposed, cudaStream_t s) {
+  if (!valid_fmt(tin) || !valid_fmt(tout) || (tin == kF16 && tout == kBF16)) return MUON_ERR_INVALID_ARG;
   CUtensorMap ma, mb;
   int st;
   if (!transposed) {  // X stored m x n: both operands K-major, 128-row boxes
-    st = make_map(&ma, X, batch, m, n, BM);
+    st = make_map(&ma, X, tin, batch, m, n, BM);
     mb = ma;
   } else {            // X stored n x m (X^T): both operands MN-major, 64 x 64 boxes
-    st = make_map(&ma, X, batch, n, m, 64);
+    st = make_map(&ma, X, tin, batch, n, m, 64);
     mb = ma;
   }
   if (st) return st;
   Params p = base_params((int)m, (int)m, (int)n, batch);
-  st = make_map(&p.tm_out, A, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (!st) st = make_map(&p.tm_out_t, A, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_NONE);
+  st = make_map(&p.tm_out, A, tout, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!st) st = make_map(&p.tm_out_t, A, tout, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st) return st;
   p.tiles_per_mat = triangle_tiles(p.tiles_m, p.tiles_n);
   p.num_tiles = (long long)p.tiles_per_mat * batch;
@@ -1072,19 +1177,27 @@ int ns_syrk(const __nv_bfloat16 *X, __nv_bfloat16 *A, int64_t batch, int64_t m, 
   p.out_ld = m;
   p.out_mat = m * m;
   p.scale = s2;
-  return transposed ? launch<EPI_SYRK, true, true>(ma, mb, p, kTraceSyrk, s)
-                    : launch<EPI_SYRK, false, false>(ma, mb, p, kTraceSyrk, s);
+  p.mul = mul;
+  if (tin == kF16)
+    return transposed ? launch<EPI_SYRK, true, true, kF16, kF16>(ma, mb, p, kTraceSyrk, s)
+                      : launch<EPI_SYRK, false, false, kF16, kF16>(ma, mb, p, kTraceSyrk, s);
+  if (tout == kF16)
+    return transposed ? launch<EPI_SYRK, true, true, kBF16, kF16>(ma, mb, p, kTraceSyrk, s)
+                      : launch<EPI_SYRK, false, false, kBF16, kF16>(ma, mb, p, kTraceSyrk, s);
+  return transposed ? launch<EPI_SYRK, true, true, kBF16, kBF16>(ma, mb, p, kTraceSyrk, s)
+                    : launch<EPI_SYRK, false, false, kBF16, kBF16>(ma, mb, p, kTraceSyrk, s);
 }
 
-int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, float b, float c, cudaStream_t s) {
+int ns_poly(const void *A, int tin, void *B, int tout, int64_t batch, int64_t m, float b, float c, cudaStream_t s) {
+  if (!valid_fmt(tin) || !valid_fmt(tout) || (tin == kBF16 && tout == kF16)) return MUON_ERR_INVALID_ARG;
   CUtensorMap ma, mb;
-  int st = make_map(&ma, A, batch, m, m, BM);
+  int st = make_map(&ma, A, tin, batch, m, m, BM);
   mb = ma;
   if (st) return st;
   Params p = base_params((int)m, (int)m, (int)m, batch);
-  st = make_map(&p.tm_src, A, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (!st) st = make_map(&p.tm_out, B, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (!st) st = make_map(&p.tm_out_t, B, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_NONE);
+  st = make_map(&p.tm_src, A, tin, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!st) st = make_map(&p.tm_out, B, tout, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!st) st = make_map(&p.tm_out_t, B, tout, batch, m, m, EPI_BOX, EPI_BOX, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st) return st;
   p.tiles_per_mat = triangle_tiles(p.tiles_m, p.tiles_n);
   p.num_tiles = (long long)p.tiles_per_mat * batch;
@@ -1096,30 +1209,32 @@ int ns_poly(const __nv_bfloat16 *A, __nv_bfloat16 *B, int64_t batch, int64_t m, 
   p.src_mat = m * m;
   p.b = b;
   p.c = c;
-  return launch<EPI_POLY, false, false>(ma, mb, p, kTracePoly, s);
+  if (tin == kBF16) return launch<EPI_POLY, false, false, kBF16, kBF16>(ma, mb, p, kTracePoly, s);
+  return tout == kBF16 ? launch<EPI_POLY, false, false, kF16, kBF16>(ma, mb, p, kTracePoly, s)
+                       : launch<EPI_POLY, false, false, kF16, kF16>(ma, mb, p, kTracePoly, s);
 }
 
 namespace {
 
-// X' = s1 (a X + B X) with X' written as Xn (+ Xn_lo), or, for EPI_APPLY,
+// X' = mul s1 (a X + B X) with X' written as Xn (+ Xn_lo), or, for EPI_APPLY,
 // folded into W' = kw W + ko bf16(X') with W in place of Xn.
-template <int EPI>
-int axpy_launch(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *Xn,
-                __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, float kw,
-                float ko, bool transposed, int trace_kind, cudaStream_t s) {
+template <int EPI, int TIN, int TOUT>
+int axpy_launch(const void *B, const void *X, const __nv_bfloat16 *X_lo, void *Xn, __nv_bfloat16 *Xn_lo,
+                int64_t batch, int64_t m, int64_t n, float a, const float *s1, float mul, float kw, float ko,
+                bool transposed, int trace_kind, cudaStream_t s) {
   CUtensorMap ma, mb;
   int st;
   Params p;
   if (!transposed) {
     // X' (m x n) = a X + B X: A operand B (K-major), B operand X (MN-major)
-    st = make_map(&ma, B, batch, m, m, BM);
-    if (!st) st = make_map(&mb, X, batch, m, n, 64);
+    st = make_map(&ma, B, TIN, batch, m, m, BM);
+    if (!st) st = make_map(&mb, X, TIN, batch, m, n, 64);
     p = base_params((int)m, (int)n, (int)m, batch);
     p.out_ld = n;
   } else {
     // X stored n x m: X'^T = a X^T + X^T B (B symmetric), both operands K-major
-    st = make_map(&ma, X, batch, n, m, BM);
-    if (!st) st = make_map(&mb, B, batch, m, m, BNH);
+    st = make_map(&ma, X, TIN, batch, n, m, BM);
+    if (!st) st = make_map(&mb, B, TIN, batch, m, m, BNH);
     p = base_params((int)n, (int)m, (int)m, batch);
     p.out_ld = m;
   }
@@ -1128,10 +1243,10 @@ int axpy_launch(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloa
   // columns, the swizzle spanning one box row
   const int eb = EPI_BOX, ecw = Layout<EPI>::cw;
   const CUtensorMapSwizzle sw64 = ecw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
-  st = make_map(&p.tm_src, X, batch, p.M, p.N, eb, ecw, sw64);
-  if (!st && X_lo) st = make_map(&p.tm_src_lo, X_lo, batch, p.M, p.N, eb, ecw, sw64);
-  if (!st) st = make_map(&p.tm_out, Xn, batch, p.M, p.N, eb, ecw, sw64);
-  if (!st && Xn_lo) st = make_map(&p.tm_out_lo, Xn_lo, batch, p.M, p.N, eb, ecw, sw64);
+  st = make_map(&p.tm_src, X, TIN, batch, p.M, p.N, eb, ecw, sw64);
+  if (!st && X_lo) st = make_map(&p.tm_src_lo, X_lo, kBF16, batch, p.M, p.N, eb, ecw, sw64);
+  if (!st) st = make_map(&p.tm_out, Xn, EPI == EPI_APPLY ? kBF16 : TOUT, batch, p.M, p.N, eb, ecw, sw64);
+  if (!st && Xn_lo) st = make_map(&p.tm_out_lo, Xn_lo, kBF16, batch, p.M, p.N, eb, ecw, sw64);
   if (st) return st;
   p.tiles_per_mat = p.tiles_m * p.tiles_n;
   p.num_tiles = (long long)p.tiles_per_mat * batch;
@@ -1142,28 +1257,41 @@ int axpy_launch(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloa
   p.src_mat = m * n;
   p.a = a;
   p.scale = s1;
+  p.mul = mul;
   p.src_lo = X_lo;
   p.out_lo = Xn_lo;
   p.kw = kw;
   p.ko = ko;
   p.row_order = transposed ? MUON_AXPY_ROW_ORDER_T : 0;
-  return transposed ? launch<EPI, false, false>(ma, mb, p, trace_kind, s)
-                    : launch<EPI, false, true>(ma, mb, p, trace_kind, s);
+  return transposed ? launch<EPI, false, false, TIN, TOUT>(ma, mb, p, trace_kind, s)
+                    : launch<EPI, false, true, TIN, TOUT>(ma, mb, p, trace_kind, s);
 }
 
 }  // namespace
 
-int ns_axpy(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *Xn,
-            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, bool transposed,
-            cudaStream_t s) {
-  return axpy_launch<EPI_AXPY>(B, X, X_lo, Xn, Xn_lo, batch, m, n, a, s1, 0.f, 0.f, transposed, kTraceAxpy, s);
+int ns_axpy(const void *B, const void *X, int tin, const __nv_bfloat16 *X_lo, void *Xn, int tout,
+            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, float mul,
+            bool transposed, cudaStream_t s) {
+  if (!valid_fmt(tin) || !valid_fmt(tout)) return MUON_ERR_INVALID_ARG;
+  if (tin == kBF16)
+    return tout == kBF16 ? axpy_launch<EPI_AXPY, kBF16, kBF16>(B, X, X_lo, Xn, Xn_lo, batch, m, n, a, s1, mul, 0.f,
+                                                               0.f, transposed, kTraceAxpy, s)
+                         : axpy_launch<EPI_AXPY, kBF16, kF16>(B, X, X_lo, Xn, Xn_lo, batch, m, n, a, s1, mul, 0.f,
+                                                              0.f, transposed, kTraceAxpy, s);
+  return tout == kBF16 ? axpy_launch<EPI_AXPY, kF16, kBF16>(B, X, X_lo, Xn, Xn_lo, batch, m, n, a, s1, mul, 0.f, 0.f,
+                                                            transposed, kTraceAxpy, s)
+                       : axpy_launch<EPI_AXPY, kF16, kF16>(B, X, X_lo, Xn, Xn_lo, batch, m, n, a, s1, mul, 0.f, 0.f,
+                                                           transposed, kTraceAxpy, s);
 }
 
-int ns_axpy_apply(const __nv_bfloat16 *B, const __nv_bfloat16 *X, const __nv_bfloat16 *X_lo, __nv_bfloat16 *W,
-                  int64_t batch, int64_t m, int64_t n, float a, const float *s1, float kw, float ko, bool transposed,
+int ns_axpy_apply(const void *B, const void *X, int tin, const __nv_bfloat16 *X_lo, __nv_bfloat16 *W, int64_t batch,
+                  int64_t m, int64_t n, float a, const float *s1, float mul, float kw, float ko, bool transposed,
                   cudaStream_t s) {
-  return axpy_launch<EPI_APPLY>(B, X, X_lo, W, nullptr, batch, m, n, a, s1, kw, ko, transposed, kTraceAxpyApply,
-                                s);
+  if (!valid_fmt(tin)) return MUON_ERR_INVALID_ARG;
+  return tin == kBF16 ? axpy_launch<EPI_APPLY, kBF16, kBF16>(B, X, X_lo, W, nullptr, batch, m, n, a, s1, mul, kw, ko,
+                                                             transposed, kTraceAxpyApply, s)
+                      : axpy_launch<EPI_APPLY, kF16, kBF16>(B, X, X_lo, W, nullptr, batch, m, n, a, s1, mul, kw, ko,
+                                                            transposed, kTraceAxpyApply, s);
 }
 
 int selftest_wait(unsigned long long timeout_ns, cudaStream_t s) {

@@ -35,25 +35,33 @@ bool is_host_accessible_pinned(const void *p) {
   return a.type == cudaMemoryTypeHost;
 }
 
+// The side streams and every event the call records, all created before any
+// device memory is allocated, so that no failure after the allocation can
+// skip the join of the side streams or the stream-ordered free.
 struct Streams {
   cudaStream_t in = nullptr, out = nullptr;
   cudaEvent_t in_done[2] = {}, compute_done[2] = {}, out_done[2] = {};
+  cudaEvent_t ready = nullptr, tail[2] = {};
   ~Streams() {
     for (int i = 0; i < 2; ++i) {
       if (in_done[i]) cudaEventDestroy(in_done[i]);
       if (compute_done[i]) cudaEventDestroy(compute_done[i]);
       if (out_done[i]) cudaEventDestroy(out_done[i]);
+      if (tail[i]) cudaEventDestroy(tail[i]);
     }
+    if (ready) cudaEventDestroy(ready);
     if (in) cudaStreamDestroy(in);    // deferred by CUDA until the enqueued work is done
     if (out) cudaStreamDestroy(out);
   }
   bool create() {
     if (cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking) != cudaSuccess) return false;
     if (cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&ready, cudaEventDisableTiming) != cudaSuccess) return false;
     for (int i = 0; i < 2; ++i)
       if (cudaEventCreateWithFlags(&in_done[i], cudaEventDisableTiming) != cudaSuccess ||
           cudaEventCreateWithFlags(&compute_done[i], cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&out_done[i], cudaEventDisableTiming) != cudaSuccess)
+          cudaEventCreateWithFlags(&out_done[i], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&tail[i], cudaEventDisableTiming) != cudaSuccess)
         return false;
     return true;
   }
@@ -85,24 +93,24 @@ extern "C" int muon_step_host(void *param_host, const void *grad_host, float *mo
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   Streams st;
-  if (!st.create()) return MUON_ERR_CUDA;
+  if (!st.create()) {
+    cudaGetLastError();
+    return MUON_ERR_CUDA;
+  }
   uint8_t *dev = nullptr;
   if (cudaMallocAsync(reinterpret_cast<void **>(&dev), 2 * slot_bytes + ws, s) != cudaSuccess || !dev) {
     cudaGetLastError();
     return MUON_ERR_NO_MEMORY;
   }
+  int status = MUON_OK;
   // the side streams must not touch the slots before the allocation is ordered
-  cudaEvent_t ready;
-  if (cudaEventCreateWithFlags(&ready, cudaEventDisableTiming) != cudaSuccess) return MUON_ERR_CUDA;
-  cudaEventRecord(ready, s);
-  cudaStreamWaitEvent(st.in, ready, 0);
-  cudaStreamWaitEvent(st.out, ready, 0);
-  cudaEventDestroy(ready);
+  if (cudaEventRecord(st.ready, s) != cudaSuccess || cudaStreamWaitEvent(st.in, st.ready, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(st.out, st.ready, 0) != cudaSuccess)
+    status = MUON_ERR_CUDA;
 
   auto *ph = static_cast<uint8_t *>(param_host);
   auto *gh = static_cast<const uint8_t *>(grad_host);
   auto *mh = reinterpret_cast<uint8_t *>(momentum_host);
-  int status = MUON_OK;
   bool used[2] = {false, false};
   for (int64_t b0 = 0, k = 0; b0 < batch && status == MUON_OK; b0 += ch, ++k) {
     const int slot = (int)(k & 1);
@@ -139,14 +147,11 @@ extern "C" int muon_step_host(void *param_host, const void *grad_host, float *mo
   }
   // the caller's stream waits for all work on both side streams (also after an
   // error, when a copy may still be in flight), then releases the device memory
-  cudaEvent_t tail[2];
   cudaStream_t side[2] = {st.in, st.out};
-  for (int i = 0; i < 2; ++i) {
-    if (cudaEventCreateWithFlags(&tail[i], cudaEventDisableTiming) != cudaSuccess) return MUON_ERR_CUDA;
-    cudaEventRecord(tail[i], side[i]);
-    cudaStreamWaitEvent(s, tail[i], 0);
-    cudaEventDestroy(tail[i]);
-  }
+  for (int i = 0; i < 2; ++i)
+    if ((cudaEventRecord(st.tail[i], side[i]) != cudaSuccess || cudaStreamWaitEvent(s, st.tail[i], 0) != cudaSuccess) &&
+        status == MUON_OK)
+      status = MUON_ERR_CUDA;
   if (cudaFreeAsync(dev, s) != cudaSuccess && status == MUON_OK) status = MUON_ERR_CUDA;
   if (status == MUON_OK && cudaGetLastError() != cudaSuccess) status = MUON_ERR_CUDA;
   return status;

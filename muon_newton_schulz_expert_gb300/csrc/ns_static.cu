@@ -49,13 +49,13 @@ int scratch_address(void **out) {
 
 extern "C" int muon_ns_batched_static(void *X, int64_t batch, int64_t m, int64_t n, int steps, const float coeffs[3],
                                       float eps, muon_stream_t stream) {
-  // argument errors and the empty batch are answered by the workspace entry
-  // point before it looks at the workspace
-  if (batch <= 0 || m < 1 || n < 1 || steps < 0 || !coeffs || !X)
-    return muon_ns_batched_ws(X, batch, m, n, steps, coeffs, eps, nullptr, 0, stream);
+  // the errors of muon_ns_batched first, in its order, then the size limit,
+  // all before any CUDA call
+  int st = muon::ns_precheck(X, batch, m, n, steps, coeffs, eps);
+  if (st != MUON_OK || batch == 0) return st;
   if (muon_ns_workspace_bytes(batch, m, n) > MUON_NS_STATIC_SCRATCH_BYTES) return MUON_ERR_NO_MEMORY;
   void *scratch = nullptr;
-  int st = scratch_address(&scratch);
+  st = scratch_address(&scratch);
   if (st != MUON_OK) return st;
   return muon_ns_batched_ws(X, batch, m, n, steps, coeffs, eps, scratch, MUON_NS_STATIC_SCRATCH_BYTES, stream);
 }

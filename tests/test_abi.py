@@ -181,3 +181,32 @@ def test_trace_without_gpu_work_is_empty(lib):
     assert lib.muon_trace_begin() == 0
     entries = (mk.TraceEntry * 4)()
     assert lib.muon_trace_end(entries, 4) == 0
+
+
+def test_static_entry_reports_the_errors_of_muon_ns_batched_first(lib):
+    # argument and shape errors come before the size limit, as in muon_ns_batched;
+    # none of these calls reaches the GPU
+    c3 = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+    P = ctypes.c_void_p(256)
+    big = 1024   # 1024 expert-sized matrices: far over the static scratch
+    assert lib.muon_ns_workspace_bytes(big, 1792, 6144) > mk.NS_STATIC_SCRATCH_BYTES
+    assert lib.muon_ns_batched_static(P, big, 1792, 6144, 5, c3, float("nan"), None) == -1
+    assert lib.muon_ns_batched_static(P, big, 1792, 6144, 1001, c3, 1e-7, None) == -1
+    assert lib.muon_ns_batched_static(P, big, 1792, 6144, 5, None, 1e-7, None) == -1
+    assert lib.muon_ns_batched_static(P, big, 7, 6144, 5, c3, 1e-7, None) == -2
+    assert lib.muon_ns_batched_static(ctypes.c_void_p(258), big, 1792, 6144, 5, c3, 1e-7, None) == -2
+    assert lib.muon_ns_batched_static(P, big, 1792, 6144, 5, c3, 1e-7, None) == -4
+    assert lib.muon_ns_batched_static(None, 0, 1792, 6144, 5, c3, 1e-7, None) == 0
+    assert lib.muon_ns_batched_static(None, -1, 1792, 6144, 5, c3, 1e-7, None) == -1
+
+
+def test_coefficients_whose_iterates_leave_the_scaled_fp16_range_are_unsupported(lib):
+    # X grows by up to 1e6 per step: after a few steps no power-of-two scale keeps
+    # its bound inside fp16, so the tensor-core path refuses before any launch
+    grow = (ctypes.c_float * 3)(1e6, 0.0, 0.0)
+    P = ctypes.c_void_p(256)
+    assert lib.muon_ns_batched(P, 1, 64, 64, 5, grow, 1e-7, None) == -2
+    assert lib.muon_ns_batched_static(P, 1, 64, 64, 5, grow, 1e-7, None) == -2
+    assert lib.muon_step_batched(P, P, P, 1, 64, 64, 0.95, 1, 5, grow, 1e-7, 0.02, 0.1, 0.0, None, 0, None) == -2
+    # the fp32 verification path has no such limit
+    assert lib.muon_ns_batched_f32(None, 0, 64, 64, 5, grow, 1e-7, None) == 0

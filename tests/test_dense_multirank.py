@@ -1,11 +1,14 @@
 """Row-sharded dense matrices over two and three gloo ranks (CPU).
 
-The data movement of dense_step (gather to the owner, scatter back) is checked
-with stand-in operations on fp32 CPU tensors: a momentum, an orthogonalisation
-stand-in that mixes every row of the full matrix (so a row landing on the wrong
-rank or in the wrong order changes the result) and an update.  Each rank's
-shards must equal the rows of the same operations applied to the full matrices
-in one process.  The library's own kernels run in tests/test_gpu_dense.py.
+The data movement of dense_step (the all-to-all to the owners, the batched
+orthogonalisation there, the all-to-all back) is checked with stand-in
+operations on fp32 CPU tensors: a momentum, an orthogonalisation stand-in that
+mixes every row of each full matrix of a batch and depends on the matrix's
+position in the batch only through its own rows (so a row landing on the wrong
+rank, in the wrong order or in the wrong matrix changes the result) and an
+update.  Each rank's shards must equal the rows of the same operations applied
+to the full matrices in one process.  The library's own kernels run in
+tests/test_gpu_dense.py.
 """
 
 import os
@@ -17,7 +20,9 @@ import torch.multiprocessing as mp
 
 from muon_newton_schulz_expert_gb300 import dense
 
-SHAPES = [(10, 6), (7, 9), (16, 4), (3, 5), (1, 4)]   # uneven splits; fewer rows than ranks (empty shards)
+# uneven splits; fewer rows than ranks (empty shards); repeated shapes, so that
+# owners batch several matrices and some owners hold none of a shape
+SHAPES = [(10, 6), (7, 9), (16, 4), (3, 5), (1, 4), (10, 6), (7, 9), (10, 6), (10, 6)]
 MU, LR = 0.9, 0.05
 
 
@@ -26,14 +31,18 @@ def _ops():
         m.mul_(MU).add_(g)
         u.copy_(g + MU * m)
 
-    def ns(x):   # a deterministic function of the whole matrix, row order included
-        w = torch.arange(1, x.shape[0] + 1, dtype=x.dtype).unsqueeze(1)
-        x.copy_(torch.flip(x, [0]) * 0.5 + (x * w).sum(0, keepdim=True) / x.shape[0])
+    def ns(x):   # on each matrix of a (batch, rows, cols) stack: a function of the whole matrix, row order included
+        assert x.dim() == 3
+        w = torch.arange(1, x.shape[1] + 1, dtype=x.dtype).view(1, -1, 1)
+        x.copy_(torch.flip(x, [1]) * 0.5 + (x * w).sum(1, keepdim=True) / x.shape[1])
 
     def apply(p, o, sc):
         p.mul_(0.99).add_(o, alpha=-LR * sc)
 
-    return dense.Ops(momentum, ns, apply)
+    def scale(r, c):
+        return 1.0 + r / (r + c)
+
+    return dense.Ops(momentum, ns, apply, scale)
 
 
 def _full_inputs(seed=7):
@@ -50,8 +59,8 @@ def _reference():
     for (r, c), p, g, m in zip(SHAPES, params, grads, moms):
         u = torch.empty_like(g)
         ops.momentum(g, m, u)
-        ops.ns(u)
-        ops.apply(p, u, dense.default_scale(r, c))
+        ops.ns(u.unsqueeze(0))
+        ops.apply(p, u, ops.scale(r, c))
     return params, moms
 
 
@@ -76,7 +85,7 @@ def _worker(rank, world, port, out):
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("world", [2, 3, 4])
 def test_dense_step_matches_the_full_matrices(world):
     port = _free_port()
     with mp.Manager() as mgr:
@@ -106,8 +115,8 @@ def test_row_splits_and_owners():
             assert all(a == b for (_, a), (b, _) in zip(s, s[1:]))
             assert max(b - a for a, b in s) - min(b - a for a, b in s) <= 1
     assert [dense.owner_of(j, 3) for j in range(5)] == [0, 1, 2, 0, 1]
-    assert dense.default_scale(6144, 1792) == pytest.approx((6144 / 1792) ** 0.5)
-    assert dense.default_scale(1792, 6144) == 1.0
+    assert dense.shape_groups(SHAPES) == [((10, 6), [0, 5, 7, 8]), ((7, 9), [1, 6]), ((16, 4), [2]), ((3, 5), [3]),
+                                          ((1, 4), [4])]
 
 
 def test_single_rank_runs_without_a_process_group():

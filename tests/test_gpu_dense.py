@@ -1,10 +1,12 @@
 """dense_step on one GPU with the library's kernels.
 
-With one rank, dense_step runs the momentum, Newton-Schulz and update calls on
-each full matrix; its result must equal, bit for bit, the fused step on the
-same matrices given the same fp32 shape scale (the dense path hands the full
-matrix's scale to the update as an fp32 argument).  The gather/scatter of more
-ranks is covered on CPU by tests/test_dense_multirank.py.
+With one rank, dense_step stacks the matrices of each shape and runs one
+batched Newton-Schulz call per shape between the momentum and update calls.
+Its result must match the fp64 oracle (momentum bit for bit, the
+orthogonalised update within 2e-2), and equal, bit for bit, the fused step on
+the same matrices given the same fp32 shape scale (the dense path hands the
+full matrix's scale to the update as an fp32 argument).  The all-to-all of
+more ranks is covered on CPU by tests/test_dense_multirank.py.
 """
 
 import numpy as np
@@ -13,11 +15,14 @@ import torch
 
 import workloads
 from muon_newton_schulz_expert_gb300 import dense
-from tests._util import bits16, bits32, require_gpu
+from oracle import muon_oracle as O
+from tests._util import bits16, bits32, np32, rel_fro, require_gpu
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(workloads.HIDDEN, workloads.HIDDEN), (workloads.HIDDEN, 1024), (264, 776), (776, 264)]
+# two matrices of the attention-like square shape, so that one call batches them
+SHAPES = [(workloads.HIDDEN, workloads.HIDDEN), (workloads.HIDDEN, 1024), (264, 776), (776, 264),
+          (workloads.HIDDEN, workloads.HIDDEN)]
 
 
 @pytest.fixture(scope="module")
@@ -40,14 +45,34 @@ def test_single_rank_dense_step_equals_fused_step(mk, scale):
     mats = _inputs(4100)
     params = [W.clone() for W, _, _ in mats]
     moms = [m.clone() for _, _, m in mats]
-    dense.dense_step(params, [g for _, g, _ in mats], moms, SHAPES, scale=scale)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    dense.dense_step(params, [g for _, g, _ in mats], moms, SHAPES, scale=scale, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     assert mk.muon_get_device_status() == 0
     for (r, c), (W, g, m), p2, m2 in zip(SHAPES, mats, params, moms):
         W1, m1 = W.clone().unsqueeze(0), m.clone().unsqueeze(0)
-        sc = scale if scale > 0 else float(np.float32(dense.default_scale(r, c)))
+        sc = scale if scale > 0 else mk.muon_default_scale(r, c)
         mk.muon_step_batched(W1, g.unsqueeze(0), m1, scale=sc)
         torch.cuda.synchronize()
         assert not torch.equal(p2, W)
         assert np.array_equal(bits32(m2), bits32(m1[0]))
         assert np.array_equal(bits16(p2), bits16(W1[0]))
+
+
+def test_single_rank_dense_step_matches_oracle(mk):
+    # W = 0, lr = 1, wd = 0, scale = 1: the new parameter is -bf16(O)
+    mats = _inputs(4200)
+    params = [torch.zeros_like(W) for W, _, _ in mats]
+    moms = [m.clone() for _, _, m in mats]
+    dense.dense_step(params, [g for _, g, _ in mats], moms, SHAPES, lr=1.0, weight_decay=0.0, scale=1.0)
+    torch.cuda.synchronize()
+    assert mk.muon_get_device_status() == 0
+    for j, ((r, c), (W, g, m), p2, m2) in enumerate(zip(SHAPES, mats, params, moms)):
+        ref = O.muon_step(np.zeros((1, r, c)), np32(g)[None], np32(m)[None], mu=float(np.float32(0.95)), lr=1.0,
+                          weight_decay=0.0, scale=1.0)
+        assert np.array_equal(bits32(m2), ref["buf"][0].view(np.uint32)), j
+        err = rel_fro(-np32(p2), ref["O"][0])
+        print(f"dense matrix {j} {r}x{c}: rel {err:.3e}")
+        assert err < 2e-2, (j, err)

@@ -50,6 +50,28 @@ def test_static_scratch_matches_allocating_entry_point_twice(mk):
         assert torch.equal(X, ref)   # same kernels, same order: identical bits
 
 
+def test_static_scratch_after_a_large_call_on_ragged_and_near_limit_shapes(mk):
+    # After a call that fills most of the scratch, calls whose tiles do not
+    # divide their shapes (TMA-clipped loads and stores near the end of the
+    # regions they use) and a call whose workspace sits just under the limit
+    # must still match the allocating entry point bit for bit: nothing a call
+    # reads is left over from an earlier one.
+    big = (1, workloads.EXPERT_HIDDEN, workloads.HIDDEN)
+    ragged = [(2, 520, 776), (3, 776, 264), (2, 8, 8)]
+    # the largest batch of 1024 x 3072 matrices whose workspace fits
+    near = max(((b, 1024, 3072) for b in range(1, 16)
+                if mk.muon_ns_workspace_bytes(b, 1024, 3072) <= mk.NS_STATIC_SCRATCH_BYTES),
+               key=lambda s: s[0])
+    assert mk.muon_ns_workspace_bytes(*near) > 0.7 * mk.NS_STATIC_SCRATCH_BYTES
+    for k, (b, m, n) in enumerate([big] + ragged + [near] + ragged[:1]):
+        X = workloads.gradients(b, m, n, 4400 + k, device="cuda")
+        ref = X.clone()
+        mk.muon_ns_batched(ref)
+        assert call_static(mk, X) == 0
+        assert mk.muon_get_device_status() == 0
+        assert torch.equal(X, ref), (b, m, n)
+
+
 def test_static_scratch_rejects_sizes_beyond_its_maximum(mk):
     X = workloads.gradients(2, workloads.EXPERT_HIDDEN, workloads.HIDDEN, 4343, device="cuda")
     before = X.clone()
