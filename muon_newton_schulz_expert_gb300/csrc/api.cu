@@ -312,6 +312,19 @@ int plan_ns(int64_t mm, int steps, const float *cf, int cf_stride, std::vector<I
   return MUON_OK;
 }
 
+// Which iterates carry X's low half.  Rounding an iterate to 16 bits adds
+// noise to every singular direction, and each later step multiplies small
+// singular values by up to a (3.4445 for the quintic), so the low half
+// matters most early: without it on the first step's output the
+// conditioning-stress inputs reach 18% error.  The last step's input is the
+// exception: its rounding passes through one step only (gain <= a), which
+// costs at most 0.3% of the output's norm on those inputs (a CPU model of the
+// rounding points, 1 to 6 steps), while dropping it saves 4 bytes per element
+// of traffic: the low half's store in the second-to-last step and its load in
+// the last.
+inline bool writes_low_half(int it, int steps) { return it + 2 < steps; }
+inline bool reads_low_half(int it, int steps) { return it > 0 && writes_low_half(it - 1, steps); }
+
 // The tensor-core iteration on the canonical orientation.  `src0` holds X
 // (bf16, mm x nn per matrix); the result (bf16) ends in `dst_final`, which may
 // be src0 itself.  Intermediate iterates live in the workspace's two X
@@ -335,8 +348,9 @@ int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *dst_final, const Workspace 
     MUON_TRY(ns_syrk(src, q.tin, w.a, q.store, batch, mm, nn, it == 0 ? w.inv2 : nullptr, q.syrk_mul, transposed, s));
     MUON_TRY(ns_poly(w.a, q.store, w.b, q.tin, batch, mm, q.poly_b, q.poly_c, s));
     // the first input is exactly bf16 (no low half); the result leaves as bf16
-    MUON_TRY(ns_axpy(w.b, src, q.tin, it == 0 ? nullptr : lo, dst, last ? kBF16 : q.store, last ? nullptr : lo, batch,
-                     mm, nn, q.axpy_a, it == 0 ? w.inv : nullptr, q.axpy_mul, transposed, s));
+    MUON_TRY(ns_axpy(w.b, src, q.tin, reads_low_half(it, steps) ? lo : nullptr, dst, last ? kBF16 : q.store,
+                     writes_low_half(it, steps) ? lo : nullptr, batch, mm, nn, q.axpy_a, it == 0 ? w.inv : nullptr,
+                     q.axpy_mul, transposed, s));
     src = dst;
   }
   if (src != dst_final) MUON_TRY(copy_async(dst_final, src, (size_t)batch * per * 2, s));
@@ -593,7 +607,7 @@ static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, cons
     const IterPlan &q = plan[it];
     MUON_TRY(ns_syrk(src, q.tin, w.a, q.store, batch, mm, nn, it == 0 ? w.inv2 : nullptr, q.syrk_mul, transposed, s));
     MUON_TRY(ns_poly(w.a, q.store, w.b, q.tin, batch, mm, q.poly_b, q.poly_c, s));
-    const __nv_bfloat16 *src_lo = it == 0 ? nullptr : lo;
+    const __nv_bfloat16 *src_lo = reads_low_half(it, steps) ? lo : nullptr;
     const float *s1 = it == 0 ? w.inv : nullptr;
     if (it == steps - 1) {
       MUON_TRY(wait_param_free(w_free, s));
@@ -601,7 +615,8 @@ static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, cons
                            s);
     }
     void *dst = src == w.x1 ? w.x2 : w.x1;
-    MUON_TRY(ns_axpy(w.b, src, q.tin, src_lo, dst, q.store, lo, batch, mm, nn, q.axpy_a, s1, q.axpy_mul, transposed, s));
+    MUON_TRY(ns_axpy(w.b, src, q.tin, src_lo, dst, q.store, writes_low_half(it, steps) ? lo : nullptr, batch, mm, nn,
+                     q.axpy_a, s1, q.axpy_mul, transposed, s));
     src = dst;
   }
   return MUON_OK;
