@@ -97,11 +97,6 @@ constexpr int UMMA_K = 16;
 #ifndef MUON_AXPY_ROW_ORDER_T
 #define MUON_AXPY_ROW_ORDER_T 1
 #endif
-// aX + BX epilogues: X's halves through shared memory by TMA (0) or through
-// registers by plain loads and stores (1)
-#ifndef MUON_AXPY_EPI_REGS
-#define MUON_AXPY_EPI_REGS 0
-#endif
 #ifndef MUON_AXPY_INPLACE
 #define MUON_AXPY_INPLACE 1
 #endif
@@ -166,12 +161,10 @@ struct Layout {
                                 : EPI == EPI_AXPY ? MUON_STAGES_AXPY
                                 : EPI == EPI_POLY ? MUON_STAGES_POLY
                                                   : MUON_STAGES_SYRK;
-  // the register epilogue of aX + BX stages nothing in shared memory
-  static constexpr int slots = EPI >= EPI_AXPY && MUON_AXPY_EPI_REGS ? 0
-                               : EPI == EPI_APPLY                    ? MUON_SLOTS_APPLY
-                               : EPI == EPI_AXPY                     ? MUON_SLOTS_AXPY
-                               : EPI == EPI_POLY                     ? MUON_SLOTS_POLY
-                                                                     : MUON_SLOTS_SYRK;
+  static constexpr int slots = EPI == EPI_APPLY  ? MUON_SLOTS_APPLY
+                               : EPI == EPI_AXPY ? MUON_SLOTS_AXPY
+                               : EPI == EPI_POLY ? MUON_SLOTS_POLY
+                                                 : MUON_SLOTS_SYRK;
   // Bytes of one input slot and of the output slot per epilogue warp.
   // SYRK/POLY: a slot is [direct box][mirror box], with no separate output.
   // AXPY: input [X hi][X lo], the result [X' hi][X' lo] written over it (or,
@@ -194,7 +187,7 @@ struct Layout {
                                                 : MUON_KSUB_SYRK;
   static constexpr int stage_bytes = ksub * STAGE_BYTES;
   static constexpr int smem_bytes = stages * stage_bytes + epi_bytes + 1024 + num_bars * 8 + 16;
-  static_assert(slots == 0 || (128 / cw) % slots == 0, "chunks per tile must fill the staging slots evenly");
+  static_assert((128 / cw) % slots == 0, "chunks per tile must fill the staging slots evenly");
   static_assert(smem_bytes <= 232448, "shared memory per CTA");
 };
 
@@ -526,24 +519,6 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
     if (global_ns() - t0 > limit_ns) return;
 }
 
-// wait_bounded, inlined: a call boundary would make the caller wait for its
-// registers' pending loads (the epilogue's prefetched operands) first.
-__device__ __forceinline__ bool wait_bounded_inl(uint32_t bar, uint32_t parity, Watch w) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*w.abort) return false;
-      if (global_ns() - t0 > w.limit_ns) {
-        *w.abort = 1;
-        atomicOr(w.err, kErrTimeout);
-        return false;
-      }
-    }
-  }
-}
-
 // TIN: the 16-bit format of both tensor-core operands (which is also that of
 // the epilogue's operand, A for POLY and X's high half for AXPY / APPLY);
 // TOUT: the format the epilogue stores (SYRK, POLY, AXPY; APPLY stores bf16).
@@ -736,116 +711,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_commit_mc(drain_bar, 0x1);
       volatile int no_abort = 0;
       wait_bounded(drain_bar, 0, Watch{&no_abort, p.err, p.timeout_ns});
-    }
-  } else if (EPI >= EPI_AXPY && MUON_AXPY_EPI_REGS) {
-    // ---------------------------------------------------------------- AXPY epilogue through registers (both CTAs)
-    // The same arithmetic as the shared-memory epilogue below, with X's halves
-    // (and APPLY's W) read straight from global memory into registers and the
-    // results stored from registers: lane i owns row i of the warp's 32 rows
-    // (TMEM lane 32q + i) and reads / writes its 32 columns of a chunk as four
-    // 16-byte pieces per matrix.  The next chunk's pieces (the next tile's
-    // first chunk at the end of a tile) are loaded before the current chunk
-    // is computed, so their latency hides behind it.
-    constexpr bool APPLY = EPI == EPI_APPLY;
-    constexpr int NCH = 4;                       // 32-column chunks per warp and tile
-    const int ew = warp - 2;
-    const int q = warp & 3, half = ew >> 2;
-    const bool lo_in = p.src_lo != nullptr, lo_out = !APPLY && p.out_lo != nullptr;
-    const int rbase = (int)rank * BM + q * 32;
-    uint4 h_cur[4], l_cur[4], w_cur[4], h_nxt[4], l_nxt[4], w_nxt[4];
-    // loads the lane's pieces of chunk (m_, row0_, col0_) into the *_nxt registers
-    auto load_chunk = [&](int m_, int row0_, int col0_) {
-      const int row = row0_ + lane;
-      const long long base = (long long)m_ * p.src_mat + (long long)row * p.src_ld;
-      const uint4 *hp = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.src) + base);
-      const uint4 *lp = reinterpret_cast<const uint4 *>(p.src_lo + base);
-      const uint4 *wp = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.out) + base);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = col0_ + 8 * j;   // N is a multiple of 8: a piece is wholly inside or outside
-        const bool in = row < p.M && c < p.N;
-        const int o = (c >> 3);
-        h_nxt[j] = in ? __ldcg(hp + o) : make_uint4(0u, 0u, 0u, 0u);
-        l_nxt[j] = in && lo_in ? __ldcg(lp + o) : make_uint4(0u, 0u, 0u, 0u);
-        if (APPLY) w_nxt[j] = in ? __ldcg(wp + o) : make_uint4(0u, 0u, 0u, 0u);
-      }
-    };
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    long long t = cid;
-    int mat = 0, ti = 0, tj = 0;
-    if (t < p.num_tiles) {
-      decode_tile<EPI>(p, t, mat, ti, tj);
-      load_chunk(mat, ti * CM + rbase, tj * BN + half * 128);
-    }
-    for (; t < p.num_tiles; t += ncl) {
-      const long long tn = t + ncl;
-      int mat_n = 0, ti_n = 0, tj_n = 0;
-      if (tn < p.num_tiles) decode_tile<EPI>(p, tn, mat_n, ti_n, tj_n);
-      const bool ok = wait_bounded_inl(ACCF(acc), acc_phase, w);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      const int row0 = ti * CM + rbase;
-      const int row = row0 + lane;
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS + half * 128);
-      const float sc = (p.scale ? p.scale[mat] : 1.0f) * p.mul;
-      const long long obase = (long long)mat * p.out_mat + (long long)row * p.out_ld;
-      uint4 *op = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + obase);
-      uint4 *olp = reinterpret_cast<uint4 *>(p.out_lo + obase);
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          h_cur[j] = h_nxt[j];
-          l_cur[j] = l_nxt[j];
-          if (APPLY) w_cur[j] = w_nxt[j];
-        }
-        const int col0 = tj * BN + half * 128 + ch * 32;
-        if (ch + 1 < NCH)
-          load_chunk(mat, row0, col0 + 32);
-        else if (tn < p.num_tiles)
-          load_chunk(mat_n, ti_n * CM + rbase, tj_n * BN + half * 128);
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(taddr + (uint32_t)(ch * 32), r);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t hv[4] = {h_cur[j].x, h_cur[j].y, h_cur[j].z, h_cur[j].w};
-          const uint32_t lv[4] = {l_cur[j].x, l_cur[j].y, l_cur[j].z, l_cur[j].w};
-          const uint32_t wv[4] = {w_cur[j].x, w_cur[j].y, w_cur[j].z, w_cur[j].w};
-          uint32_t ho[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k = j * 8 + 2 * e;
-            const float2 fh = unpack2<TIN>(hv[e]), fl = unpack2<kBF16>(lv[e]);
-            const float v0 = sc * fmaf(p.a, fh.x + fl.x, __uint_as_float(r[k]));
-            const float v1 = sc * fmaf(p.a, fh.y + fl.y, __uint_as_float(r[k + 1]));
-            if (APPLY) {  // O = bf16(X'); W' = kw W + ko O, each product and the sum rounded separately
-              const float2 hh = unpack2<kBF16>(pack2<kBF16>(v0, v1));
-              const float2 wf = unpack2<kBF16>(wv[e]);
-              ho[e] = pack2<kBF16>(__fadd_rn(__fmul_rn(p.kw, wf.x), __fmul_rn(p.ko, hh.x)),
-                                   __fadd_rn(__fmul_rn(p.kw, wf.y), __fmul_rn(p.ko, hh.y)));
-            } else {
-              ho[e] = pack2<TOUT>(v0, v1);
-              const float2 hh = unpack2<TOUT>(ho[e]);
-              lo[e] = pack2<kBF16>(v0 - hh.x, v1 - hh.y);
-            }
-          }
-          const int c = col0 + 8 * j;
-          if (row < p.M && c < p.N) {
-            op[c >> 3] = make_uint4(ho[0], ho[1], ho[2], ho[3]);
-            if (lo_out) olp[c >> 3] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(map_to_rank(ACCE(acc), 0));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-      mat = mat_n;
-      ti = ti_n;
-      tj = tj_n;
     }
   } else if (EPI >= EPI_AXPY) {
     // ---------------------------------------------------------------- AXPY epilogue (both CTAs)
