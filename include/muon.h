@@ -48,7 +48,7 @@ typedef struct CUevent_st *muon_event_t;
 typedef enum {
   MUON_OK = 0,
   MUON_ERR_INVALID_ARG = -1,  /* null pointer, negative size, bad coefficient pointer ... */
-  MUON_ERR_UNSUPPORTED = -2,  /* shape or alignment the bf16 tensor-core path does not take */
+  MUON_ERR_UNSUPPORTED = -2,  /* shape, alignment or coefficients the tensor-core path does not take */
   MUON_ERR_CUDA = -3,         /* a CUDA runtime call or kernel launch failed */
   MUON_ERR_NO_MEMORY = -4,    /* workspace allocation failed or workspace too small */
   MUON_ERR_TIMEOUT = -5,      /* a device-side bounded wait ran out (kernel returned early) */
