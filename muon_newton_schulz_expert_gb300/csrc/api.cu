@@ -123,8 +123,8 @@ int num_sms() {
 namespace {
 
 // Workspace of one Newton-Schulz call on [batch][mm][nn] (mm <= nn), in order:
-// two X buffers, the low half of X (tensor-core path only), A, B (mm x mm
-// each), norm partials, 1/(||X||+eps) and its square.  Every region starts on
+// two X buffers, the low half of X (tensor-core path only, one byte per
+// element), A, B (mm x mm each), norm partials, 1/(||X||+eps) and its square.  Every region starts on
 // a 256-byte boundary and is followed by kGapBytes that no kernel writes, so
 // that a write past a region's end lands in a gap a test can inspect rather
 // than in the next region.
@@ -137,11 +137,19 @@ constexpr size_t kGapBytes = 256;
 
 inline size_t region(size_t bytes) { return align256(bytes) + kGapBytes; }
 
+// X's low half, one byte per element, rows padded to 16 bytes (TMA strides):
+// room for either storage orientation
+inline size_t pitch16(int64_t cols) { return (size_t)((cols + 15) & ~int64_t(15)); }
+inline size_t lo_bytes(int64_t batch, int64_t mm, int64_t nn) {
+  return (size_t)batch * std::max((size_t)mm * pitch16(nn), (size_t)nn * pitch16(mm));
+}
+
 size_t ws_bytes(int64_t batch, int64_t mm, int64_t nn, size_t elem) {
   const size_t xs = region((size_t)batch * mm * nn * elem);
+  const size_t los = elem == 2 ? region(lo_bytes(batch, mm, nn)) : 0;
   const size_t as = region((size_t)batch * mm * mm * elem);
   const size_t fl = region((size_t)batch * norm_partials() * sizeof(float)) + 2 * region((size_t)batch * sizeof(float));
-  return (elem == 2 ? 3 : 2) * xs + 2 * as + fl;
+  return 2 * xs + los + 2 * as + fl;
 }
 
 Workspace carve(void *base, int64_t batch, int64_t mm, int64_t nn, size_t elem) {
@@ -155,7 +163,7 @@ Workspace carve(void *base, int64_t batch, int64_t mm, int64_t nn, size_t elem) 
   p += xs;
   if (elem == 2) {
     w.lo = p;
-    p += xs;
+    p += region(lo_bytes(batch, mm, nn));
   }
   w.a = p;
   p += as;
@@ -226,6 +234,7 @@ struct IterPlan {
   float syrk_mul;          // sigma_A / sigma_in^2
   float poly_b, poly_c;    // b sigma_B / sigma_A, c sigma_B / sigma_A^2
   float axpy_a, axpy_mul;  // a sigma_B, sigma_out / (sigma_in sigma_B)
+  float lo_in, lo_out;     // the low half's power-of-two factors: read (1/S) and written (S)
   int tin;                 // format of X and B in this iteration's product
   int store;               // format of A, and of B and X' unless bf16 is required
 };
@@ -281,22 +290,46 @@ bool storage_exp(double bound, int *e) {
   return true;
 }
 
+// X's low half, lo = x - hi with hi = x rounded to the storage format, is at
+// most hi's rounding unit: |lo| <= 2^-8 |x| for bf16 (2^-11 for fp16), with
+// x the stored value sigma X'.  It is kept in 8 bits as e5m2(lo * S) (five
+// exponent bits, two of mantissa, finite up to 57344), S a power of two that
+// puts the bound at 2^13 or below; e5m2's 31 binades below that keep every
+// lo that matters (a CPU model of these rounding points puts the cost at
+// <= 0.5% of the output's norm on the conditioning-stress inputs, against a
+// 16-bit low half).
+bool low_half_scale(double bound, int *e) {
+  if (!(bound > 1e-30)) {
+    *e = 0;
+    return true;
+  }
+  if (!std::isfinite(bound)) return false;
+  const int k = 13 - (int)ceil(log2(bound * 1.01));
+  *e = std::max(-100, std::min(100, k));
+  return true;
+}
+
 int plan_ns(int64_t mm, int steps, const float *cf, int cf_stride, std::vector<IterPlan> *plan) {
   plan->assign((size_t)steps, IterPlan{});
   const int store = mm <= kF16MaxRows ? kF16 : kBF16;
   double bx = 1.0;   // bound on ||X_k||
   int ex = 0;        // sigma_X of the current input (the first input carries s instead)
+  int elo = 0;       // S of the current input's low half
   for (int it = 0; it < steps; ++it) {
     const double a = cf[(size_t)it * cf_stride], b = cf[(size_t)it * cf_stride + 1],
                  c = cf[(size_t)it * cf_stride + 2];
+    const double bx_next = max_abs_quintic(a, b, c, bx);
     int ea = 0, eb = 0, eo = 0;
     if (store == kF16) {   // bf16 shares fp32's exponent range: no scaling
       const double ba = bx * bx, bb = max_abs_quad(b, c, ba);
-      const double bx_next = max_abs_quintic(a, b, c, bx);
       if (!storage_exp(ba, &ea)) return MUON_ERR_UNSUPPORTED;
       if (it > 0 && !storage_exp(bb, &eb)) return MUON_ERR_UNSUPPORTED;   // the first B is bf16
       if (it + 1 < steps && !storage_exp(bx_next, &eo)) return MUON_ERR_UNSUPPORTED;
-      bx = bx_next;
+    }
+    int elo_out = 0;
+    if (it + 1 < steps) {
+      const double unit = store == kF16 ? ldexp(1.0, -11) : ldexp(1.0, -8);
+      if (!low_half_scale(unit * ldexp(bx_next, eo), &elo_out)) return MUON_ERR_UNSUPPORTED;
     }
     const int ein = it == 0 ? 0 : ex;
     IterPlan &q = (*plan)[it];
@@ -305,9 +338,13 @@ int plan_ns(int64_t mm, int steps, const float *cf, int cf_stride, std::vector<I
     q.poly_c = (float)ldexp(c, eb - 2 * ea);
     q.axpy_a = (float)ldexp(a, eb);
     q.axpy_mul = (float)ldexp(1.0, eo - ein - eb);   // the last iteration stores the value itself
+    q.lo_in = (float)ldexp(1.0, -elo);
+    q.lo_out = (float)ldexp(1.0, elo_out);
     q.tin = it == 0 ? kBF16 : store;
     q.store = store;
+    bx = bx_next;
     ex = eo;
+    elo = elo_out;
   }
   return MUON_OK;
 }
@@ -337,7 +374,7 @@ int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *dst_final, const Workspace 
   MUON_TRY(plan_ns(mm, steps, cf, cf_stride, &plan));
   MUON_TRY(launch_inv_norm_bf16(src0, batch, per, eps, w.partial, w.inv, w.inv2, s));
   if (steps == 0) return launch_scale_bf16(src0, dst_final, batch, per, w.inv, s);
-  auto *lo = static_cast<__nv_bfloat16 *>(w.lo);
+  auto *lo = static_cast<uint8_t *>(w.lo);
   void *src = src0;
   for (int it = 0; it < steps; ++it) {
     const IterPlan &q = plan[it];
@@ -348,9 +385,9 @@ int ns_bf16_core(__nv_bfloat16 *src0, __nv_bfloat16 *dst_final, const Workspace 
     MUON_TRY(ns_syrk(src, q.tin, w.a, q.store, batch, mm, nn, it == 0 ? w.inv2 : nullptr, q.syrk_mul, transposed, s));
     MUON_TRY(ns_poly(w.a, q.store, w.b, q.tin, batch, mm, q.poly_b, q.poly_c, s));
     // the first input is exactly bf16 (no low half); the result leaves as bf16
-    MUON_TRY(ns_axpy(w.b, src, q.tin, reads_low_half(it, steps) ? lo : nullptr, dst, last ? kBF16 : q.store,
-                     writes_low_half(it, steps) ? lo : nullptr, batch, mm, nn, q.axpy_a, it == 0 ? w.inv : nullptr,
-                     q.axpy_mul, transposed, s));
+    MUON_TRY(ns_axpy(w.b, src, q.tin, reads_low_half(it, steps) ? lo : nullptr, q.lo_in, dst, last ? kBF16 : q.store,
+                     writes_low_half(it, steps) ? lo : nullptr, q.lo_out, batch, mm, nn, q.axpy_a,
+                     it == 0 ? w.inv : nullptr, q.axpy_mul, transposed, s));
     src = dst;
   }
   if (src != dst_final) MUON_TRY(copy_async(dst_final, src, (size_t)batch * per * 2, s));
@@ -595,7 +632,7 @@ static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, cons
   std::vector<IterPlan> plan;
   MUON_TRY(plan_ns(mm, steps, cf0, cf_stride, &plan));
   auto *x2 = static_cast<__nv_bfloat16 *>(w.x2);
-  auto *lo = static_cast<__nv_bfloat16 *>(w.lo);
+  auto *lo = static_cast<uint8_t *>(w.lo);
   MUON_TRY(launch_momentum_norm_bf16(G, mom, x2, batch, per, mu, nesterov, eps, w.partial, w.inv, w.inv2, s));
   if (steps == 0) {
     MUON_TRY(launch_scale_bf16(x2, x2, batch, per, w.inv, s));
@@ -607,16 +644,15 @@ static int step_fused(__nv_bfloat16 *W, const __nv_bfloat16 *G, float *mom, cons
     const IterPlan &q = plan[it];
     MUON_TRY(ns_syrk(src, q.tin, w.a, q.store, batch, mm, nn, it == 0 ? w.inv2 : nullptr, q.syrk_mul, transposed, s));
     MUON_TRY(ns_poly(w.a, q.store, w.b, q.tin, batch, mm, q.poly_b, q.poly_c, s));
-    const __nv_bfloat16 *src_lo = reads_low_half(it, steps) ? lo : nullptr;
+    const uint8_t *src_lo = reads_low_half(it, steps) ? lo : nullptr;
     const float *s1 = it == 0 ? w.inv : nullptr;
-    if (it == steps - 1) {
+    if (it == steps - 1) {   // the last iteration's input carries no low half
       MUON_TRY(wait_param_free(w_free, s));
-      return ns_axpy_apply(w.b, src, q.tin, src_lo, W, batch, mm, nn, q.axpy_a, s1, q.axpy_mul, kw, ko, transposed,
-                           s);
+      return ns_axpy_apply(w.b, src, q.tin, W, batch, mm, nn, q.axpy_a, s1, q.axpy_mul, kw, ko, transposed, s);
     }
     void *dst = src == w.x1 ? w.x2 : w.x1;
-    MUON_TRY(ns_axpy(w.b, src, q.tin, src_lo, dst, q.store, writes_low_half(it, steps) ? lo : nullptr, batch, mm, nn,
-                     q.axpy_a, s1, q.axpy_mul, transposed, s));
+    MUON_TRY(ns_axpy(w.b, src, q.tin, src_lo, q.lo_in, dst, q.store, writes_low_half(it, steps) ? lo : nullptr,
+                     q.lo_out, batch, mm, nn, q.axpy_a, s1, q.axpy_mul, transposed, s));
     src = dst;
   }
   return MUON_OK;

@@ -92,7 +92,7 @@ int launch_scale_f32(const float *src, float *dst, int64_t batch, int64_t per, c
 // 16-bit storage formats: the caller's matrices are bf16; what the iteration
 // produces is stored in bf16 or in fp16 scaled by powers of two (see plan_ns
 // in api.cu).
-enum Fmt16 : int { kBF16 = 0, kF16 = 1 };
+enum Fmt16 : int { kBF16 = 0, kF16 = 1, kE5M2 = 2 /* X's 8-bit low half only */ };
 // All matrices are batched, densely packed, row-major; X is m x n (m <= n),
 // stored as m x n or, with `transposed`, as its transpose (n x m).
 // A = tout(mul * s2[b] * X X^T)   (s2 == nullptr: 1), upper triangle computed,
@@ -103,19 +103,18 @@ int ns_syrk(const void *X, int tin, void *A, int tout, int64_t batch, int64_t m,
 // mirrored (bf16 A gives bf16 B)
 int ns_poly(const void *A, int tin, void *B, int tout, int64_t batch, int64_t m, float b, float c, cudaStream_t s);
 // Xn = tout(mul * s1[b] * (a*X + B X))   (s1 == nullptr: 1), with X = X + X_lo
-// (B and X of format tin, X_lo bf16) and the result split into Xn and
-// Xn_lo = bf16(result - Xn); X_lo and Xn_lo may be null (zero low half / not
-// wanted) and may be the same buffer (all of X, X_lo, Xn, Xn_lo in the same
-// storage orientation)
-int ns_axpy(const void *B, const void *X, int tin, const __nv_bfloat16 *X_lo, void *Xn, int tout,
-            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, float mul,
+// (B and X of format tin; X_lo e5m2 bytes times lo_in_mul) and the result
+// split into Xn and Xn_lo = e5m2((result - Xn) * lo_out_mul); X_lo and Xn_lo
+// may be null (zero low half / not wanted) and may be the same buffer (all
+// of X, X_lo, Xn, Xn_lo in the same storage orientation)
+int ns_axpy(const void *B, const void *X, int tin, const uint8_t *X_lo, float lo_in_mul, void *Xn, int tout,
+            uint8_t *Xn_lo, float lo_out_mul, int64_t batch, int64_t m, int64_t n, float a, const float *s1, float mul,
             bool transposed, cudaStream_t s);
-// The last iteration with the parameter update fused in: O = bf16(mul * s1[b]
-// * (a*X + B X)) is not stored; W = bf16(kw*W + ko*O) in place, with W (bf16)
-// stored in the same orientation as X.
-int ns_axpy_apply(const void *B, const void *X, int tin, const __nv_bfloat16 *X_lo, __nv_bfloat16 *W, int64_t batch,
-                  int64_t m, int64_t n, float a, const float *s1, float mul, float kw, float ko, bool transposed,
-                  cudaStream_t s);
+// The last iteration with the parameter update fused in (its input carries no
+// low half): O = bf16(mul * s1[b] * (a*X + B X)) is not stored; W = bf16(kw*W +
+// ko*O) in place, with W (bf16) stored in the same orientation as X.
+int ns_axpy_apply(const void *B, const void *X, int tin, __nv_bfloat16 *W, int64_t batch, int64_t m, int64_t n,
+                  float a, const float *s1, float mul, float kw, float ko, bool transposed, cudaStream_t s);
 int selftest_wait(unsigned long long timeout_ns, cudaStream_t s);
 
 // ---- fp32 SIMT GEMMs for the verification mode (gemm_f32.cu) ----

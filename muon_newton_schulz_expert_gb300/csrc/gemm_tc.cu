@@ -58,6 +58,7 @@
 // rate does not depend on how many pairs run, so L2 reads are not the limit).
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <mutex>
 
@@ -96,9 +97,6 @@ constexpr int UMMA_K = 16;
 #endif
 #ifndef MUON_AXPY_ROW_ORDER_T
 #define MUON_AXPY_ROW_ORDER_T 1
-#endif
-#ifndef MUON_AXPY_INPLACE
-#define MUON_AXPY_INPLACE 1
 #endif
 #ifndef MUON_KSUB_SYRK
 #define MUON_KSUB_SYRK 1
@@ -165,20 +163,18 @@ struct Layout {
                                : EPI == EPI_AXPY ? MUON_SLOTS_AXPY
                                : EPI == EPI_POLY ? MUON_SLOTS_POLY
                                                  : MUON_SLOTS_SYRK;
-  // Bytes of one input slot and of the output slot per epilogue warp.
-  // SYRK/POLY: a slot is [direct box][mirror box], with no separate output.
-  // AXPY: input [X hi][X lo], the result [X' hi][X' lo] written over it (or,
-  // with MUON_AXPY_INPLACE 0, into an output box of its own); APPLY: input
-  // [X hi][X lo][W] of cw-column boxes, W' written over it.
+  // Bytes of one slot per epilogue warp.  SYRK/POLY: [direct box][mirror box].
+  // AXPY: [X hi][X lo] (lo one byte per element), the result [X' hi][X' lo]
+  // written over it; APPLY: [X hi][W] of cw-column boxes, W' written over it.
   // epilogue chunk width in columns (boxes of 32 rows x cw)
   static constexpr int cw = EPI == EPI_APPLY ? MUON_APPLY_CW : 32;
   static_assert(cw == 32 || cw == 16, "epilogue chunks of 32 or 16 columns");
   static constexpr int box_bytes = 32 * cw * 2;
-  static constexpr int in_bytes = (EPI == EPI_APPLY ? 3 : 2) * box_bytes;
+  static constexpr int lo_bytes = 32 * cw;
+  static constexpr int in_bytes = EPI == EPI_APPLY ? 2 * box_bytes : EPI == EPI_AXPY ? box_bytes + lo_bytes : EPI_BUF;
   static_assert(EPI >= EPI_AXPY || in_bytes == EPI_BUF, "the symmetric epilogues address slots of EPI_BUF bytes");
-  static constexpr bool inplace = (EPI == EPI_AXPY && MUON_AXPY_INPLACE != 0) || EPI == EPI_APPLY;
-  static constexpr int out_bytes = inplace ? 0 : EPI == EPI_APPLY ? box_bytes : EPI == EPI_AXPY ? 2 * box_bytes : 0;
-  static constexpr int epi_bytes = EPI_WARPS * (slots * in_bytes + out_bytes);
+  static_assert(in_bytes % 1024 == 0, "slots keep the boxes' swizzle alignment");
+  static constexpr int epi_bytes = EPI_WARPS * slots * in_bytes;
   static constexpr int num_bars = 2 * stages + 5 + EPI_WARPS * slots;
   // k-blocks of 64 per stage (one barrier round trip per ksub k-blocks)
   static constexpr int ksub = EPI == EPI_APPLY  ? MUON_KSUB_APPLY
@@ -207,10 +203,12 @@ struct Params {
   long long src_ld, src_mat;
   const float *scale;          // per-matrix factor (SYRK: s^2, AXPY: s) or null
   float mul;                   // SYRK, AXPY: power-of-two storage factor, times scale[mat]
-  // AXPY only: low halves of X (X = hi + lo, hi = bf16(X), lo = bf16(X - hi));
-  // read at the element the thread then writes, so one buffer serves in place
-  const __nv_bfloat16 *src_lo;
-  __nv_bfloat16 *out_lo;
+  // AXPY only: low halves of X as e5m2 bytes, lo = e5m2 * lo_in_mul on the way
+  // in and e5m2(lo' * lo_out_mul) on the way out (powers of two); read at the
+  // element the thread then writes, so one buffer serves in place
+  const uint8_t *src_lo;
+  uint8_t *out_lo;
+  float lo_in_mul, lo_out_mul;
   float a, b, c;               // AXPY: a; POLY: b, c (with the storage factors folded in)
   float kw, ko;                // APPLY only: W' = kw W + ko O
   unsigned *err;
@@ -459,6 +457,22 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
     __half2 h = *reinterpret_cast<__half2 *>(&v);
     return __half22float2(h);
   }
+}
+
+// The two e5m2 bytes in half `hi16` of `word` (first in the low byte) as two
+// floats times `mul`.  e5m2 is the upper byte of an IEEE fp16, so the bytes
+// widen exactly through fp16.
+__device__ __forceinline__ float2 e5m2x2_to_float2(uint32_t word, int hi16, float mul) {
+  const uint32_t pair = hi16 ? (word >> 16) : (word & 0xffffu);
+  const uint32_t h2 = __byte_perm(pair, 0u, 0x1404);   // [0, b0, 0, b1]: fp16 pair (b0 << 8, b1 << 8)
+  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+  return make_float2(f.x * mul, f.y * mul);
+}
+
+// Two floats to two e5m2 bytes (round to nearest even, saturating to the
+// largest finite value), the first in the low byte.
+__device__ __forceinline__ uint32_t float2_to_e5m2x2(float x, float y) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E5M2);
 }
 
 // One float to the 16-bit pattern of format T.
@@ -715,42 +729,44 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (EPI >= EPI_AXPY) {
     // ---------------------------------------------------------------- AXPY epilogue (both CTAs)
     // X' = s (a (hi + lo) + acc) through shared memory: each warp stages a
-    // 32 x 32 box of hi and of lo (TMA load, zero-filled past the edges),
-    // writes hi' = TOUT(X'), lo' = bf16(X' - hi') over it (each lane over
-    // what it has just read) and TMA-stores it (clipped at the edges); the
-    // boxes of chunk g + SLOTS are fetched into the slot once that store has
-    // read it.  APPLY also stages the box of W and writes W' = bf16(kw W +
-    // ko bf16(X')), the parameter update of the unfused path, operation for
-    // operation, over the slot, in chunks of MUON_APPLY_CW columns (three
-    // 2 KB boxes, or 1 KB ones for 16 columns).  Lane i owns row i of the box,
-    // which is TMEM lane 32q + i; the swizzle spanning a box row (64 or 32
-    // bytes) makes these row reads conflict-free.
+    // 32 x 32 box of hi and the matching 32 x 32 bytes of lo (TMA loads,
+    // zero-filled past the edges), writes hi' = TOUT(X') and lo' = e5m2(S_out
+    // (X' - hi')) over them (each lane over what it has just read) and
+    // TMA-stores them (clipped at the edges); the boxes of chunk g + SLOTS are
+    // fetched into the slot once those stores have read it.  lo is stored as
+    // an 8-bit e5m2 times a power of two: X' - hi' is at most hi's rounding
+    // unit, which a bound on X' limits, so the scale S_out keeps every lo' in
+    // e5m2's range (and lo = e5m2 / S_in on the way in).  APPLY stages hi and
+    // the box of W instead (the last iteration's input carries no low half)
+    // and writes W' = bf16(kw W + ko bf16(X')), the parameter update of the
+    // unfused path, operation for operation, over the slot, in chunks of
+    // MUON_APPLY_CW columns (2 KB boxes, or 1 KB ones for 16 columns).  Lane i
+    // owns row i of the box, which is TMEM lane 32q + i; the swizzle spanning a
+    // box row (64 or 32 bytes) makes these row reads conflict-free.
     constexpr bool APPLY = EPI == EPI_APPLY;
-    constexpr bool INPLACE = Layout<EPI>::inplace;
     constexpr int SLOTS = Layout<EPI>::slots;
     constexpr int IN_BYTES = Layout<EPI>::in_bytes;
     constexpr int CW = Layout<EPI>::cw;            // chunk width: 32 columns, or 16
     constexpr int NCH = 128 / CW;                  // chunks per warp and tile
-    constexpr int BOXB = Layout<EPI>::box_bytes;   // one 32 x CW box
-    constexpr int PIECES = CW / 8;                 // 16-byte pieces per box row
+    constexpr int BOXB = Layout<EPI>::box_bytes;   // one 32 x CW box of 16-bit values
+    constexpr int LOB = Layout<EPI>::lo_bytes;     // one 32 x CW box of the 8-bit low half
+    constexpr int PIECES = CW / 8;                 // 16-byte pieces per 16-bit box row
+    static_assert(APPLY || CW == 32, "aX + BX moves 32-column chunks");
     const int ew = warp - 2;
     const int q = warp & 3, half = ew >> 2;
-    // SLOTS input slots, then the output slot
-    uint8_t *ebase = epi_smem + ew * (SLOTS * IN_BYTES + Layout<EPI>::out_bytes);
+    uint8_t *ebase = epi_smem + ew * SLOTS * IN_BYTES;
     const uint32_t ebase_s = smem_u32(ebase);
-    uint8_t *obuf = ebase + SLOTS * IN_BYTES;
-    const uint32_t obuf_s = ebase_s + SLOTS * IN_BYTES;
     uint32_t ephase_bits = 0;                                // parity per slot
     uint32_t pending = 0;                                    // slots with a load not yet waited for
-    const bool lo_in = p.src_lo != nullptr, lo_out = !APPLY && p.out_lo != nullptr;
-    const uint32_t etx = (lo_in ? 2u : 1u) * BOXB + (APPLY ? (uint32_t)BOXB : 0u);
+    const bool lo_in = !APPLY && p.src_lo != nullptr, lo_out = !APPLY && p.out_lo != nullptr;
+    const uint32_t etx = BOXB + (lo_in ? (uint32_t)LOB : 0u) + (APPLY ? (uint32_t)BOXB : 0u);
     auto epi_load = [&](int slot, int m_, int row0_, int col0_) {  // lane 0 only
       const uint32_t dst = ebase_s + slot * IN_BYTES, bar = EBAR(ew * SLOTS + slot);
       fence_proxy_async_smem();
       mbar_expect_tx(bar, etx);
       tma_load_3d(dst, &p.tm_src, bar, col0_, row0_, m_);
       if (lo_in) tma_load_3d(dst + BOXB, &p.tm_src_lo, bar, col0_, row0_, m_);
-      if (APPLY) tma_load_3d(dst + 2 * BOXB, &p.tm_out, bar, col0_, row0_, m_);  // W, stored over later
+      if (APPLY) tma_load_3d(dst + BOXB, &p.tm_out, bar, col0_, row0_, m_);  // W, stored over later
       pending |= 1u << slot;
     };
     const int rbase = (int)rank * BM + q * 32;  // this warp's rows within a pair tile
@@ -778,6 +794,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int ch = 0; ch < NCH; ++ch) {
         const int slot = ch % SLOTS;   // NCH is a multiple of SLOTS
         uint8_t *ebuf = ebase + slot * IN_BYTES;
+        const uint32_t ebuf_s = ebase_s + slot * IN_BYTES;
         const int col0 = tj * BN + half * 128 + ch * CW;
         const bool got = wait_bounded(EBAR(ew * SLOTS + slot), (ephase_bits >> slot) & 1u, w);
         if (!__all_sync(0xffffffffu, got)) {
@@ -792,46 +809,70 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(taddr + (uint32_t)(ch * CW), r);
         else
           tmem_ld16(taddr + (uint32_t)(ch * CW), r);
-        if (!INPLACE && lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the output box
         __syncwarp();
-        uint8_t *ob = INPLACE ? ebuf : obuf;
-        const uint32_t ob_s = INPLACE ? ebase_s + slot * IN_BYTES : obuf_s;
+        if (APPLY) {
 #pragma unroll
-        for (int c = 0; c < PIECES; ++c) {
-          // 64-byte rows with the 64-byte swizzle, or 32-byte rows with the 32-byte swizzle
-          const uint32_t off = CW == 32 ? (uint32_t)(lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4))
-                                        : (uint32_t)(lane * 32 + ((c ^ ((lane >> 2) & 1)) << 4));
-          Pack8 hv, lv, wv, ho, lo;
-          hv.v = *reinterpret_cast<const uint4 *>(ebuf + off);
-          lv.v = lo_in ? *reinterpret_cast<const uint4 *>(ebuf + BOXB + off) : make_uint4(0u, 0u, 0u, 0u);
-          if (APPLY) wv.v = *reinterpret_cast<const uint4 *>(ebuf + 2 * BOXB + off);
+          for (int c = 0; c < PIECES; ++c) {
+            // 64-byte rows with the 64-byte swizzle, or 32-byte rows with the 32-byte swizzle
+            const uint32_t off = CW == 32 ? (uint32_t)(lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4))
+                                          : (uint32_t)(lane * 32 + ((c ^ ((lane >> 2) & 1)) << 4));
+            Pack8 hv, wv, ho;
+            hv.v = *reinterpret_cast<const uint4 *>(ebuf + off);
+            wv.v = *reinterpret_cast<const uint4 *>(ebuf + BOXB + off);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k = c * 8 + 2 * e;
-            const float2 fh = unpack2<TIN>(hv.w[e]), fl = unpack2<kBF16>(lv.w[e]);
-            const float v0 = sc * fmaf(p.a, fh.x + fl.x, __uint_as_float(r[k]));
-            const float v1 = sc * fmaf(p.a, fh.y + fl.y, __uint_as_float(r[k + 1]));
-            if (APPLY) {  // O = bf16(X'); W' = kw W + ko O, each product and the sum rounded separately
+            for (int e = 0; e < 4; ++e) {
+              const int k = c * 8 + 2 * e;
+              const float2 fh = unpack2<TIN>(hv.w[e]);
+              const float v0 = sc * fmaf(p.a, fh.x, __uint_as_float(r[k]));
+              const float v1 = sc * fmaf(p.a, fh.y, __uint_as_float(r[k + 1]));
+              // O = bf16(X'); W' = kw W + ko O, each product and the sum rounded separately
               const float2 hh = unpack2<kBF16>(pack2<kBF16>(v0, v1));
               const float2 wf = unpack2<kBF16>(wv.w[e]);
               ho.w[e] = pack2<kBF16>(__fadd_rn(__fmul_rn(p.kw, wf.x), __fmul_rn(p.ko, hh.x)),
                                      __fadd_rn(__fmul_rn(p.kw, wf.y), __fmul_rn(p.ko, hh.y)));
-            } else {
-              ho.w[e] = pack2<TOUT>(v0, v1);
-              const float2 hh = unpack2<TOUT>(ho.w[e]);
-              lo.w[e] = pack2<kBF16>(v0 - hh.x, v1 - hh.y);
             }
+            *reinterpret_cast<uint4 *>(ebuf + off) = ho.v;
           }
-          *reinterpret_cast<uint4 *>(ob + off) = ho.v;
-          if (lo_out) *reinterpret_cast<uint4 *>(ob + BOXB + off) = lo.v;
+        } else {
+          // two 16-byte pieces of lo per lane row (32 bytes, 32-byte swizzle), each
+          // covering two 16-byte pieces of hi (8 columns each)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t loff = (uint32_t)(lane * 32 + ((j ^ ((lane >> 2) & 1)) << 4));
+            Pack8 lv, lo;
+            lv.v = lo_in ? *reinterpret_cast<const uint4 *>(ebuf + BOXB + loff) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int c = 2 * j + cc;
+              const uint32_t off = (uint32_t)(lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
+              Pack8 hv, ho;
+              hv.v = *reinterpret_cast<const uint4 *>(ebuf + off);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int k = c * 8 + 2 * e;
+                const float2 fh = unpack2<TIN>(hv.w[e]);
+                const float2 fl = e5m2x2_to_float2(lv.w[cc * 2 + (e >> 1)], e & 1, p.lo_in_mul);
+                const float v0 = sc * fmaf(p.a, fh.x + fl.x, __uint_as_float(r[k]));
+                const float v1 = sc * fmaf(p.a, fh.y + fl.y, __uint_as_float(r[k + 1]));
+                ho.w[e] = pack2<TOUT>(v0, v1);
+                const float2 hh = unpack2<TOUT>(ho.w[e]);
+                const uint32_t l2 = float2_to_e5m2x2((v0 - hh.x) * p.lo_out_mul, (v1 - hh.y) * p.lo_out_mul);
+                // bytes 2e, 2e+1 of this hi piece's 8 lo bytes
+                const int word = cc * 2 + (e >> 1);
+                lo.w[word] = (e & 1) ? (lo.w[word] & 0x0000ffffu) | (l2 << 16) : l2;
+              }
+              *reinterpret_cast<uint4 *>(ebuf + off) = ho.v;
+            }
+            if (lo_out) *reinterpret_cast<uint4 *>(ebuf + BOXB + loff) = lo.v;
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_3d(&p.tm_out, ob_s, col0, row0, mat);
-          if (lo_out) tma_store_3d(&p.tm_out_lo, ob_s + BOXB, col0, row0, mat);
+          tma_store_3d(&p.tm_out, ebuf_s, col0, row0, mat);
+          if (lo_out) tma_store_3d(&p.tm_out_lo, ebuf_s + BOXB, col0, row0, mat);
           bulk_commit();
-          if (INPLACE) bulk_wait_read_all();  // the store has read the slot the next load fills
+          bulk_wait_read_all();  // the stores have read the slot the next load fills
           // every lane has read this input slot: fetch chunk ch + SLOTS into it (possibly of the next tile)
           const int nc = ch + SLOTS;
           if (nc < NCH)
@@ -1072,17 +1113,22 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D map over a dense [batch][rows][cols] stack of 16-bit elements of format
-// `fmt`; box = box_cols columns x box_rows rows x 1 matrix.
+// 3-D map over a [batch][rows][cols] stack of elements of format `fmt`
+// (16-bit, or the 8-bit low half), rows `pitch` elements apart (0: dense);
+// box = box_cols columns x box_rows rows x 1 matrix.
 int make_map(CUtensorMap *map, const void *base, int fmt, int64_t batch, int64_t rows, int64_t cols, int box_rows,
-             int box_cols = 64, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+             int box_cols = 64, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, int64_t pitch = 0) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return MUON_ERR_CUDA;
+  const cuuint64_t es = fmt == kE5M2 ? 1 : 2;   // element bytes
+  const cuuint64_t ld = (cuuint64_t)(pitch > 0 ? pitch : cols);
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
-  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(rows * cols * 2)};
+  cuuint64_t strides[2] = {ld * es, (cuuint64_t)rows * ld * es};
   cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  const CUtensorMapDataType dt = fmt == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = fmt == kE5M2 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : fmt == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUresult r = enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MUON_OK : MUON_ERR_CUDA;
@@ -1219,9 +1265,9 @@ namespace {
 // X' = mul s1 (a X + B X) with X' written as Xn (+ Xn_lo), or, for EPI_APPLY,
 // folded into W' = kw W + ko bf16(X') with W in place of Xn.
 template <int EPI, int TIN, int TOUT>
-int axpy_launch(const void *B, const void *X, const __nv_bfloat16 *X_lo, void *Xn, __nv_bfloat16 *Xn_lo,
-                int64_t batch, int64_t m, int64_t n, float a, const float *s1, float mul, float kw, float ko,
-                bool transposed, int trace_kind, cudaStream_t s) {
+int axpy_launch(const void *B, const void *X, const uint8_t *X_lo, float lo_in_mul, void *Xn, uint8_t *Xn_lo,
+                float lo_out_mul, int64_t batch, int64_t m, int64_t n, float a, const float *s1, float mul, float kw,
+                float ko, bool transposed, int trace_kind, cudaStream_t s) {
   CUtensorMap ma, mb;
   int st;
   Params p;
@@ -1244,9 +1290,14 @@ int axpy_launch(const void *B, const void *X, const __nv_bfloat16 *X_lo, void *X
   const int eb = EPI_BOX, ecw = Layout<EPI>::cw;
   const CUtensorMapSwizzle sw64 = ecw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
   st = make_map(&p.tm_src, X, TIN, batch, p.M, p.N, eb, ecw, sw64);
-  if (!st && X_lo) st = make_map(&p.tm_src_lo, X_lo, kBF16, batch, p.M, p.N, eb, ecw, sw64);
+  // the low half: one byte per element, rows padded to 16 bytes (TMA strides);
+  // boxes of 32 rows x 32 bytes, the 32-byte swizzle spanning a row
+  const int64_t lo_pitch = (p.N + 15) & ~int64_t(15);
+  if (!st && X_lo)
+    st = make_map(&p.tm_src_lo, X_lo, kE5M2, batch, p.M, p.N, eb, 32, CU_TENSOR_MAP_SWIZZLE_32B, lo_pitch);
   if (!st) st = make_map(&p.tm_out, Xn, EPI == EPI_APPLY ? kBF16 : TOUT, batch, p.M, p.N, eb, ecw, sw64);
-  if (!st && Xn_lo) st = make_map(&p.tm_out_lo, Xn_lo, kBF16, batch, p.M, p.N, eb, ecw, sw64);
+  if (!st && Xn_lo)
+    st = make_map(&p.tm_out_lo, Xn_lo, kE5M2, batch, p.M, p.N, eb, 32, CU_TENSOR_MAP_SWIZZLE_32B, lo_pitch);
   if (st) return st;
   p.tiles_per_mat = p.tiles_m * p.tiles_n;
   p.num_tiles = (long long)p.tiles_per_mat * batch;
@@ -1260,6 +1311,8 @@ int axpy_launch(const void *B, const void *X, const __nv_bfloat16 *X_lo, void *X
   p.mul = mul;
   p.src_lo = X_lo;
   p.out_lo = Xn_lo;
+  p.lo_in_mul = lo_in_mul;
+  p.lo_out_mul = lo_out_mul;
   p.kw = kw;
   p.ko = ko;
   p.row_order = transposed ? MUON_AXPY_ROW_ORDER_T : 0;
@@ -1269,29 +1322,25 @@ int axpy_launch(const void *B, const void *X, const __nv_bfloat16 *X_lo, void *X
 
 }  // namespace
 
-int ns_axpy(const void *B, const void *X, int tin, const __nv_bfloat16 *X_lo, void *Xn, int tout,
-            __nv_bfloat16 *Xn_lo, int64_t batch, int64_t m, int64_t n, float a, const float *s1, float mul,
+int ns_axpy(const void *B, const void *X, int tin, const uint8_t *X_lo, float lo_in_mul, void *Xn, int tout,
+            uint8_t *Xn_lo, float lo_out_mul, int64_t batch, int64_t m, int64_t n, float a, const float *s1, float mul,
             bool transposed, cudaStream_t s) {
   if (!valid_fmt(tin) || !valid_fmt(tout)) return MUON_ERR_INVALID_ARG;
-  if (tin == kBF16)
-    return tout == kBF16 ? axpy_launch<EPI_AXPY, kBF16, kBF16>(B, X, X_lo, Xn, Xn_lo, batch, m, n, a, s1, mul, 0.f,
-                                                               0.f, transposed, kTraceAxpy, s)
-                         : axpy_launch<EPI_AXPY, kBF16, kF16>(B, X, X_lo, Xn, Xn_lo, batch, m, n, a, s1, mul, 0.f,
-                                                              0.f, transposed, kTraceAxpy, s);
-  return tout == kBF16 ? axpy_launch<EPI_AXPY, kF16, kBF16>(B, X, X_lo, Xn, Xn_lo, batch, m, n, a, s1, mul, 0.f, 0.f,
-                                                            transposed, kTraceAxpy, s)
-                       : axpy_launch<EPI_AXPY, kF16, kF16>(B, X, X_lo, Xn, Xn_lo, batch, m, n, a, s1, mul, 0.f, 0.f,
-                                                           transposed, kTraceAxpy, s);
+#define MUON_AXPY(TI, TO)                                                                                          \
+  axpy_launch<EPI_AXPY, TI, TO>(B, X, X_lo, lo_in_mul, Xn, Xn_lo, lo_out_mul, batch, m, n, a, s1, mul, 0.f, 0.f, \
+                                transposed, kTraceAxpy, s)
+  if (tin == kBF16) return tout == kBF16 ? MUON_AXPY(kBF16, kBF16) : MUON_AXPY(kBF16, kF16);
+  return tout == kBF16 ? MUON_AXPY(kF16, kBF16) : MUON_AXPY(kF16, kF16);
+#undef MUON_AXPY
 }
 
-int ns_axpy_apply(const void *B, const void *X, int tin, const __nv_bfloat16 *X_lo, __nv_bfloat16 *W, int64_t batch,
-                  int64_t m, int64_t n, float a, const float *s1, float mul, float kw, float ko, bool transposed,
-                  cudaStream_t s) {
+int ns_axpy_apply(const void *B, const void *X, int tin, __nv_bfloat16 *W, int64_t batch, int64_t m, int64_t n,
+                  float a, const float *s1, float mul, float kw, float ko, bool transposed, cudaStream_t s) {
   if (!valid_fmt(tin)) return MUON_ERR_INVALID_ARG;
-  return tin == kBF16 ? axpy_launch<EPI_APPLY, kBF16, kBF16>(B, X, X_lo, W, nullptr, batch, m, n, a, s1, mul, kw, ko,
-                                                             transposed, kTraceAxpyApply, s)
-                      : axpy_launch<EPI_APPLY, kF16, kBF16>(B, X, X_lo, W, nullptr, batch, m, n, a, s1, mul, kw, ko,
-                                                            transposed, kTraceAxpyApply, s);
+  return tin == kBF16 ? axpy_launch<EPI_APPLY, kBF16, kBF16>(B, X, nullptr, 1.f, W, nullptr, 1.f, batch, m, n, a, s1,
+                                                             mul, kw, ko, transposed, kTraceAxpyApply, s)
+                      : axpy_launch<EPI_APPLY, kF16, kBF16>(B, X, nullptr, 1.f, W, nullptr, 1.f, batch, m, n, a, s1,
+                                                            mul, kw, ko, transposed, kTraceAxpyApply, s);
 }
 
 int selftest_wait(unsigned long long timeout_ns, cudaStream_t s) {

@@ -3,9 +3,10 @@
 Each caller buffer (X, or the fused step's parameters, gradients and
 momentum) and the workspace sit inside a larger allocation whose surrounding
 bytes hold a sentinel; inside the workspace, the library leaves an unwritten
-gap after every region (the workspace layout: two X buffers, X's low half,
-A, B, the norm partials and two per-matrix factors, each on a 256-byte
-boundary and followed by 256 bytes).  After each call every byte
+gap after every region (the workspace layout: two X buffers, X's low half
+(one byte per element, rows padded to 16 bytes), A, B, the norm partials and
+two per-matrix factors, each on a 256-byte boundary and followed by 256
+bytes).  After each call every byte
 outside what the call may write must still hold the sentinel.  The shapes
 have ragged tiles in both orientations (TMA-clipped stores, the mirrored
 transpose stores, the diagonal element stores), sizes on both sides of the
@@ -50,7 +51,9 @@ def untouched(t):
 def ws_regions(batch, m, n):
     """[(offset, bytes a call may write, bytes of the region with its padding and gap)]."""
     mm, nn = min(m, n), max(m, n)
-    sizes = [batch * mm * nn * 2] * 3 + [batch * mm * mm * 2] * 2 + [batch * 64 * 4, batch * 4, batch * 4]
+    p16 = lambda c: (c + 15) // 16 * 16     # the low half's rows are padded to 16 bytes
+    lo = batch * max(mm * p16(nn), nn * p16(mm))
+    sizes = [batch * mm * nn * 2] * 2 + [lo] + [batch * mm * mm * 2] * 2 + [batch * 64 * 4, batch * 4, batch * 4]
     out, off = [], 0
     for sz in sizes:
         out.append((off, sz, a256(sz) + GAP))

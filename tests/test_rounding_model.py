@@ -9,12 +9,15 @@ matrix) and why the formats were chosen.  The products themselves are taken
 exact (the tensor cores accumulate in fp32); what is modelled is the rounding
 of what each step stores:
 
-* bf16 scheme: A, B and X's high half in bf16, X's low half in bf16 (what
-  the library does for matrices of more than 256 rows);
+* bf16 scheme: A, B and X's high half in bf16 (what the library does for
+  matrices of more than 256 rows);
 * fp16 scheme (matrices of up to 256 rows): A, B and X's high half in fp16
   after scaling by a power of two that puts the largest possible entry near
   2^14, except the first step's B in bf16 (it meets the bf16 input in one
-  product), and X's low half in bf16.
+  product).
+In both, X's low half is kept as an 8-bit e5m2 times a power of two chosen
+from the bound on the high half's rounding unit, and the last step's input
+carries no low half, as in the library.
 The output is rounded to bf16 in both.  On 8 x 8 inputs the bf16 scheme
 exceeds the 2e-2 relative Frobenius tolerance on some inputs, while the fp16
 scheme stays well inside it; above a few dozen rows the bf16 scheme's error
@@ -47,6 +50,13 @@ def sigma_for(bound):
     return 2.0 ** (14 - math.ceil(math.log2(bound * 1.01))) if bound > 1e-30 else 1.0
 
 
+def rnd_e5m2(x, bound):
+    # e5m2(x * S) / S with S the power of two that puts `bound` at or below 2^13
+    S = 2.0 ** (13 - math.ceil(math.log2(bound * 1.01)))
+    t = torch.from_numpy(np.asarray(x * S, np.float32)).to(torch.float8_e5m2)
+    return t.to(torch.float32).double().numpy() / S
+
+
 def model(G, scheme, steps=5, coeffs=O.QUINTIC, eps=1e-7):
     X0 = np.asarray(G, np.float64)
     tr = X0.shape[0] > X0.shape[1]
@@ -70,7 +80,8 @@ def model(G, scheme, steps=5, coeffs=O.QUINTIC, eps=1e-7):
             out = rnd_bf16(Xn)
             return out.T if tr else out
         hi = rnd_bf16(Xn) if scheme == "bf16" else rnd_f16(Xn, sigma_for(bx))
-        lo = rnd_bf16(Xn - hi)
+        unit = 2.0 ** -8 if scheme == "bf16" else 2.0 ** -11
+        lo = rnd_e5m2(Xn - hi, unit * bx) if it + 2 < steps else np.zeros_like(hi)
 
 
 def rel(x, y):
