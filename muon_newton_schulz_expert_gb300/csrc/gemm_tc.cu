@@ -75,21 +75,22 @@ constexpr int BK = 64;     // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
 // Operand ring and epilogue staging share the CTA's shared memory.
 //  - A stage holds KSUB k-blocks of 64 (32 KB per k-block: 128 rows of A and
-//    a 128-row half of B) behind one full/empty barrier pair.  Each handoff
-//    (MMA commit -> producer refill -> TMA completion -> MMA issue) has a
-//    fixed cost, so two k-blocks per stage (8 MMAs per handoff) run the
-//    mainloop 4-9% faster than one where three such stages fit.  With the
-//    ring waits polled (wait_polled) the handoff is cheap enough that X X^T
-//    and the update-fused aX + BX run single stages, with more latency cover
-//    in the same bytes: six in X X^T (1% faster), five beside the update
-//    epilogue's 48 KB of slots (3.5% faster).
-//  - A stage completes only when its slowest sector arrives, so the ring must
-//    hold ~160-192 KB in flight to ride out L2/DRAM latency.
-//  - Epilogue slots: one slot = two or three 2 KB boxes per epilogue warp.
-//    X X^T: one slot (output staging).  bA + cAA: one slot (b*A in, result
-//    over it).  aX + BX: one slot of X's halves, the result written over it,
-//    so 3 double stages fit.  aX + BX with the update: one slot of three
-//    2 KB boxes (X hi, X lo, W), W' written over them.
+//    a 128-row half of B) behind one empty barrier and one full barrier per
+//    k-block.  Each handoff (MMA commit -> producer refill -> TMA completion
+//    -> MMA issue) has a fixed cost, so two k-blocks per stage (8 MMAs per
+//    refill) run aX + BX and bA + cAA faster than single stages in the same
+//    bytes (3% and 1%, measured with six single stages); the MMAs of a
+//    stage's first k-block start as soon as its own bytes land (aX + BX 1.5%
+//    faster than one full barrier per stage).  X X^T (long K) and the
+//    update-fused aX + BX run single stages: six in X X^T, five beside the
+//    update epilogue's slots.
+//  - Each TMA round trip takes ~2000-2500 SM cycles under load, so the ring
+//    must hold ~160-192 KB in flight to cover it.
+//  - Epilogue slots, one per epilogue warp.  X X^T: output staging (direct
+//    and mirror boxes).  bA + cAA: b*A in, result over it.  aX + BX: a 2 KB
+//    box of X's high half and 1 KB of its 8-bit low half, the result written
+//    over them, so 3 double stages fit.  aX + BX with the update: 2 KB boxes
+//    of X's high half and W, W' written over them.
 // aX + BX with the update: epilogue chunk width, 32 columns, or 16 (1 KB
 // boxes, so that three double stages fit beside the slot)
 #ifndef MUON_APPLY_CW
@@ -175,13 +176,15 @@ struct Layout {
   static_assert(EPI >= EPI_AXPY || in_bytes == EPI_BUF, "the symmetric epilogues address slots of EPI_BUF bytes");
   static_assert(in_bytes % 1024 == 0, "slots keep the boxes' swizzle alignment");
   static constexpr int epi_bytes = EPI_WARPS * slots * in_bytes;
-  static constexpr int num_bars = 2 * stages + 5 + EPI_WARPS * slots;
   // k-blocks of 64 per stage (one barrier round trip per ksub k-blocks)
   static constexpr int ksub = EPI == EPI_APPLY  ? MUON_KSUB_APPLY
                               : EPI == EPI_AXPY ? MUON_KSUB_AXPY
                               : EPI == EPI_POLY ? MUON_KSUB_POLY
                                                 : MUON_KSUB_SYRK;
   static constexpr int stage_bytes = ksub * STAGE_BYTES;
+  // a full barrier per k-block of each stage, an empty one per stage, two
+  // accumulator pairs, the drain barrier and one per epilogue slot
+  static constexpr int num_bars = stages * ksub + stages + 5 + EPI_WARPS * slots;
   static constexpr int smem_bytes = stages * stage_bytes + epi_bytes + 1024 + num_bars * 8 + 16;
   static_assert((128 / cw) % slots == 0, "chunks per tile must fill the staging slots evenly");
   static_assert(smem_bytes <= 232448, "shared memory per CTA");
@@ -556,17 +559,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();          // 0: issues the MMAs; 1: its peer
   const long long cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
-#define FULL(s) (bar0 + 8u * (uint32_t)(s))
-#define EMPTY(s) (bar0 + 8u * (uint32_t)(STAGES + (s)))
-#define ACCF(a) (bar0 + 8u * (uint32_t)(2 * STAGES + (a)))
-#define ACCE(a) (bar0 + 8u * (uint32_t)(2 * STAGES + 2 + (a)))
-#define EBAR(e) (bar0 + 8u * (uint32_t)(2 * STAGES + 5 + (e)))
-  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
+  constexpr int NFULL = STAGES * KSUB;
+#define FULL(s, j) (bar0 + 8u * (uint32_t)((s) * KSUB + (j)))
+#define EMPTY(s) (bar0 + 8u * (uint32_t)(NFULL + (s)))
+#define ACCF(a) (bar0 + 8u * (uint32_t)(NFULL + STAGES + (a)))
+#define ACCE(a) (bar0 + 8u * (uint32_t)(NFULL + STAGES + 2 + (a)))
+#define EBAR(e) (bar0 + 8u * (uint32_t)(NFULL + STAGES + 5 + (e)))
+  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(NFULL + STAGES + 4);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(FULL(s), 1);    // used in CTA 0: its producer's expect_tx for both halves
-      mbar_init(EMPTY(s), 1);   // multicast commit
+      for (int j = 0; j < KSUB; ++j)
+        mbar_init(FULL(s, j), 1);  // used in CTA 0: its producer's expect_tx for both halves
+      mbar_init(EMPTY(s), 1);      // multicast commit
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(ACCF(a), 1);                 // multicast commit
@@ -628,11 +633,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           const int valid = num_kb - i * KSUB < KSUB ? num_kb - i * KSUB : KSUB;
-          // CTA 0's barrier counts the bytes of both halves; CTA 1's loads only
-          // complete bytes on it (a stage is refilled only after the MMAs that
-          // read it finished, so no load can run ahead into the next phase)
-          const uint32_t full0 = map_to_rank(FULL(stage), 0);
-          if (rank == 0) mbar_expect_tx(FULL(stage), 2 * valid * STAGE_BYTES);
+          // Each k-block of the stage completes on its own full barrier, so the
+          // MMAs start on the first while the second is still landing.  CTA 0's
+          // barrier counts the bytes of both halves; CTA 1's loads only complete
+          // bytes on it (a stage is refilled only after the MMAs that read it
+          // finished, so no load can run ahead into the next phase).  A k-block
+          // past the end of K still completes its phase, with no bytes.
+          if (rank == 0)
+#pragma unroll
+            for (int j = 0; j < KSUB; ++j) mbar_expect_tx(FULL(stage, j), j < valid ? 2 * STAGE_BYTES : 0);
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
 #pragma unroll
@@ -641,6 +650,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int ki = i * KSUB + j;
             const int kb = kb0 + ki < num_kb ? kb0 + ki : kb0 + ki - num_kb;
             const uint32_t sa = sbase + stage * SBYTES + j * STAGE_BYTES, sb = sa + A_STAGE;
+            const uint32_t full0 = map_to_rank(FULL(stage, j), 0);
             // K-major operands: one box of 128 rows x 64 K-columns.  MN-major
             // operands: boxes of 64 M/N-columns x 64 K-rows, one per swizzle atom.
             if (!A_MN) {
@@ -665,13 +675,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (!ok) break;
       }
-      // After an abort, stages may still be filling.  CTA 0's full barrier of
-      // a stage counts both CTAs' bytes of every fill CTA 0 posted, so waiting
+      // After an abort, stages may still be filling.  CTA 0's full barriers of
+      // a stage count both CTAs' bytes of every fill CTA 0 posted, so waiting
       // for the last fill of each stage to complete (at once when it already
       // did) keeps both CTAs' shared memory alive until those copies land.
       if (*abort_flag && rank == 0)
         for (int s2 = 0; s2 < STAGES; ++s2)
-          if (issued & (1u << s2)) drain_wait(FULL(s2), (issued_parity >> s2) & 1u, drain_ns);
+          if (issued & (1u << s2))
+            for (int j = 0; j < KSUB; ++j) drain_wait(FULL(s2, j), (issued_parity >> s2) & 1u, drain_ns);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (CTA 0 of the pair)
@@ -687,15 +698,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t d = tmem + (uint32_t)(acc * ACC_COLS);
         bool ok = true;
         for (int i = 0; i < num_steps; ++i) {  // i-th stage of the tile in the producer's order
-          if (!wait_polled(FULL(stage), phase, w)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           const int valid = num_kb - i * KSUB < KSUB ? num_kb - i * KSUB : KSUB;
 #pragma unroll
           for (int j = 0; j < KSUB; ++j) {
             if (j >= valid) break;
+            if (!wait_polled(FULL(stage, j), phase, w)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
             const uint32_t sa = sbase + stage * SBYTES + j * STAGE_BYTES, sb = sa + A_STAGE;
 #pragma unroll
             for (int kk = 0; kk < BK / UMMA_K; ++kk) {
@@ -710,6 +721,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               tc_mma(d, adesc, bdesc, idesc, ((i * KSUB + j) | kk) != 0 ? 1u : 0u);
             }
           }
+          if (!ok) break;
           tc_commit_mc(EMPTY(stage), 0x3);  // both CTAs may refill this stage
           if (++stage == STAGES) {
             stage = 0;
