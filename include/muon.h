@@ -309,6 +309,17 @@ int muon_selftest_wait_timeout(uint64_t timeout_ns, muon_stream_t stream);
 /* Number of kernels this library has launched in this process. */
 int64_t muon_launch_count(void);
 
+/* Fault injection on the host, for testing callers' error paths: the next
+ * `count` device allocations the library makes for itself (the workspaces of
+ * muon_ns_batched, muon_ns_batched_f32, the schedule variants and
+ * muon_step_batched, and the slots of muon_step_host) fail as if the memory
+ * pool were exhausted, without calling CUDA: the call returns
+ * MUON_ERR_NO_MEMORY before it launches anything or touches its buffers.
+ * count = 0 switches it off; count < 0 is MUON_ERR_INVALID_ARG.  Returns the
+ * number of injected failures still pending before this call (>= 0).  Makes
+ * no CUDA call. */
+int muon_inject_alloc_failures(int count);
+
 /* Tracing: between muon_trace_begin() and muon_trace_end(), every kernel
  * launch is bracketed by two CUDA events recorded on its own stream.
  * muon_trace_end() synchronises those events and fills up to max_entries

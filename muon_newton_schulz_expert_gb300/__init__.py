@@ -73,6 +73,7 @@ SIGNATURES = {
     "muon_set_wait_timeout_ns": (_U64, [_U64]),
     "muon_selftest_wait_timeout": (_INT, [_U64, _P]),
     "muon_launch_count": (_I64, []),
+    "muon_inject_alloc_failures": (_INT, [_INT]),
     "muon_trace_begin": (_INT, []),
     "muon_trace_end": (_INT, [ctypes.POINTER(TraceEntry), _INT]),
 }
@@ -403,6 +404,15 @@ def muon_selftest_wait_timeout(timeout_ns, stream=None):
 
 def muon_launch_count():
     return int(lib().muon_launch_count())
+
+
+def muon_inject_alloc_failures(count):
+    """Make the library's next `count` device allocations fail (host-side fault
+    injection); returns how many were still pending."""
+    r = int(lib().muon_inject_alloc_failures(int(count)))
+    if r < 0:
+        _check("muon_inject_alloc_failures", r)
+    return r
 
 
 def muon_trace_begin():

@@ -30,6 +30,7 @@ unsigned *g_err_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int64_t> g_launches{0};
+std::atomic<int> g_fail_allocs{0};   // injected allocation failures still pending
 
 const char *kTraceNames[kTraceKinds] = {"momentum_bf16", "momentum_f32", "norm_partial", "norm_final",
                                         "transpose",     "scale",        "ns_syrk_tc",   "ns_poly_tc",
@@ -118,6 +119,13 @@ int num_sms() {
     g_sms[d] = v;
   }
   return g_sms[d];
+}
+
+cudaError_t alloc_async(void **ptr, size_t bytes, cudaStream_t s) {
+  int pending = g_fail_allocs.load();
+  while (pending > 0)
+    if (g_fail_allocs.compare_exchange_weak(pending, pending - 1)) return cudaErrorMemoryAllocation;
+  return cudaMallocAsync(ptr, bytes, s);
 }
 
 namespace {
@@ -452,7 +460,7 @@ int ns_bf16_alloc(void *X, int64_t batch, int64_t m, int64_t n, int steps, const
   MUON_TRY(plan_ns(std::min(m, n), steps, cf, cf_stride, &plan));
   const size_t bytes = ws_bytes(batch, std::min(m, n), std::max(m, n), 2);
   void *ws = nullptr;
-  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess || !ws) {
+  if (alloc_async(&ws, bytes, s) != cudaSuccess || !ws) {
     cudaGetLastError();
     return MUON_ERR_NO_MEMORY;
   }
@@ -467,7 +475,7 @@ int ns_f32_alloc(float *X, int64_t batch, int64_t m, int64_t n, int steps, const
   if (batch == 0) return MUON_OK;
   const size_t bytes = ws_bytes(batch, std::min(m, n), std::max(m, n), 4);
   void *ws = nullptr;
-  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess || !ws) {
+  if (alloc_async(&ws, bytes, s) != cudaSuccess || !ws) {
     cudaGetLastError();
     return MUON_ERR_NO_MEMORY;
   }
@@ -679,7 +687,7 @@ static int step_fused_entry(void *param, const void *grad, float *momentum, int6
   float kw, ko;
   update_constants(rows, cols, lr, weight_decay, scale, &kw, &ko);
   void *ws = workspace;
-  if (!ws && (cudaMallocAsync(&ws, need, s) != cudaSuccess || !ws)) {
+  if (!ws && (alloc_async(&ws, need, s) != cudaSuccess || !ws)) {
     cudaGetLastError();
     return MUON_ERR_NO_MEMORY;
   }
@@ -797,6 +805,11 @@ int muon_selftest_wait_timeout(uint64_t timeout_ns, muon_stream_t stream) {
 }
 
 int64_t muon_launch_count(void) { return g_launches.load(); }
+
+int muon_inject_alloc_failures(int count) {
+  if (count < 0) return MUON_ERR_INVALID_ARG;
+  return g_fail_allocs.exchange(count);
+}
 
 int muon_trace_begin(void) {
   std::lock_guard<std::mutex> lk(g_mu);

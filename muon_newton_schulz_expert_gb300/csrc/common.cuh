@@ -44,6 +44,10 @@ unsigned *device_error_word();
 unsigned long long wait_timeout_ns();
 int num_sms();
 
+// The library's own device allocations (stream-ordered on s): fails without a
+// CUDA call while injected failures are pending (muon_inject_alloc_failures).
+cudaError_t alloc_async(void **ptr, size_t bytes, cudaStream_t s);
+
 // The argument, shape and coefficient checks of muon_ns_batched, in its order,
 // without any CUDA call: MUON_OK when the call can go ahead.
 int ns_precheck(const void *X, int64_t batch, int64_t m, int64_t n, int steps, const float *coeffs, float eps);

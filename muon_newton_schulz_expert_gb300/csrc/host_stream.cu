@@ -98,7 +98,7 @@ extern "C" int muon_step_host(void *param_host, const void *grad_host, float *mo
     return MUON_ERR_CUDA;
   }
   uint8_t *dev = nullptr;
-  if (cudaMallocAsync(reinterpret_cast<void **>(&dev), 2 * slot_bytes + ws, s) != cudaSuccess || !dev) {
+  if (alloc_async(reinterpret_cast<void **>(&dev), 2 * slot_bytes + ws, s) != cudaSuccess || !dev) {
     cudaGetLastError();
     return MUON_ERR_NO_MEMORY;
   }

@@ -210,3 +210,11 @@ def test_coefficients_whose_iterates_leave_the_scaled_fp16_range_are_unsupported
     assert lib.muon_step_batched(P, P, P, 1, 64, 64, 0.95, 1, 5, grow, 1e-7, 0.02, 0.1, 0.0, None, 0, None) == -2
     # the fp32 verification path has no such limit
     assert lib.muon_ns_batched_f32(None, 0, 64, 64, 5, grow, 1e-7, None) == 0
+
+
+def test_allocation_failure_injection_counts_on_the_host(lib):
+    # the hook only sets a counter (no CUDA call); the GPU test checks its effect
+    assert lib.muon_inject_alloc_failures(2) == 0
+    assert lib.muon_inject_alloc_failures(0) == 2
+    assert lib.muon_inject_alloc_failures(-1) == -1        # MUON_ERR_INVALID_ARG
+    assert lib.muon_inject_alloc_failures(0) == 0
