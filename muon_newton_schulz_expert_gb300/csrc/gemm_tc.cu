@@ -76,14 +76,13 @@ constexpr int UMMA_K = 16;
 // Operand ring and epilogue staging share the CTA's shared memory.
 //  - A stage holds KSUB k-blocks of 64 (32 KB per k-block: 128 rows of A and
 //    a 128-row half of B) behind one empty barrier and one full barrier per
-//    k-block.  Each handoff (MMA commit -> producer refill -> TMA completion
-//    -> MMA issue) has a fixed cost, so two k-blocks per stage (8 MMAs per
-//    refill) run aX + BX and bA + cAA faster than single stages in the same
-//    bytes (3% and 1%, measured with six single stages); the MMAs of a
-//    stage's first k-block start as soon as its own bytes land (aX + BX 1.5%
-//    faster than one full barrier per stage).  X X^T (long K) and the
-//    update-fused aX + BX run single stages: six in X X^T, five beside the
-//    update epilogue's slots.
+//    k-block.  Each refill (MMA commit -> producer wait -> TMA issue) has a
+//    fixed cost, so every kernel runs three stages of two k-blocks (8 MMAs per
+//    refill); the MMAs of a stage's first k-block start as soon as its own
+//    bytes land.  Measured against one full barrier per double stage, aX + BX
+//    ran 1.5% faster; against six single stages in the same bytes (which cost
+//    a refill per k-block), the update-fused aX + BX 5.6% faster (five single
+//    stages before), aX + BX 3%, bA + cAA 1% and X X^T 1.1%.
 //  - Each TMA round trip takes ~2000-2500 SM cycles under load, so the ring
 //    must hold ~160-192 KB in flight to cover it.
 //  - Epilogue slots, one per epilogue warp.  X X^T: output staging (direct
@@ -91,8 +90,8 @@ constexpr int UMMA_K = 16;
 //    box of X's high half and 1 KB of its 8-bit low half, the result written
 //    over them, so 3 double stages fit.  aX + BX with the update: 2 KB boxes
 //    of X's high half and W, W' written over them.
-// aX + BX with the update: epilogue chunk width, 32 columns, or 16 (1 KB
-// boxes, so that three double stages fit beside the slot)
+// aX + BX with the update: epilogue chunk width, 32 columns (2 KB boxes), or
+// 16 (1 KB boxes)
 #ifndef MUON_APPLY_CW
 #define MUON_APPLY_CW 32
 #endif
@@ -100,7 +99,7 @@ constexpr int UMMA_K = 16;
 #define MUON_AXPY_ROW_ORDER_T 1
 #endif
 #ifndef MUON_KSUB_SYRK
-#define MUON_KSUB_SYRK 1
+#define MUON_KSUB_SYRK 2
 #endif
 #ifndef MUON_KSUB_POLY
 #define MUON_KSUB_POLY 2
@@ -109,10 +108,10 @@ constexpr int UMMA_K = 16;
 #define MUON_KSUB_AXPY 2
 #endif
 #ifndef MUON_KSUB_APPLY
-#define MUON_KSUB_APPLY 1
+#define MUON_KSUB_APPLY 2
 #endif
 #ifndef MUON_STAGES_SYRK
-#define MUON_STAGES_SYRK 6
+#define MUON_STAGES_SYRK 3
 #endif
 #ifndef MUON_SLOTS_SYRK
 #define MUON_SLOTS_SYRK 1
@@ -130,7 +129,7 @@ constexpr int UMMA_K = 16;
 #define MUON_SLOTS_AXPY 1
 #endif
 #ifndef MUON_STAGES_APPLY
-#define MUON_STAGES_APPLY 5
+#define MUON_STAGES_APPLY 3
 #endif
 #ifndef MUON_SLOTS_APPLY
 #define MUON_SLOTS_APPLY 1
