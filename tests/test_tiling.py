@@ -16,6 +16,15 @@ that row is computed twice or lies below the diagonal; with T even that holds
 for every odd r, T/2 rows, and each discarded block serves one row.  So no
 arrangement of pair units (any rows, any columns, any order) computes fewer
 than T/2 discarded blocks, which is what the diagonal tiles discard.
+
+The bound holds even when a block below the diagonal may stand in for its
+mirror above it (the epilogue could store it transposed).  Count, for each
+block index v, the computed off-diagonal blocks (v, w) or (w, v): every block
+pair {v, w} must be computed once, so without waste v's count is T - 1, odd
+for T even.  A unit {r0, r1} x {c0, c1} whose four blocks are all needed
+contributes an even count to every index (a 4-cycle r0-c0-r1-c1, or a loop
+and a triangle when r0 = c0), and only a block computed twice can make one
+odd, at its two indices.  T odd counts need at least T/2 such blocks.
 """
 
 import pytest
@@ -70,3 +79,77 @@ def test_no_unit_arrangement_beats_the_parity_bound_on_small_triangles():
         if best is not None:
             break
     assert best == T // 2
+
+
+def test_mirrored_blocks_do_not_beat_the_parity_bound_on_small_triangles():
+    # exhaustive for T = 4 with the mirror allowed: a unit's block (r, c) serves
+    # the pair {r, c} whichever side of the diagonal it lies on
+    import itertools
+    T = 4
+    need = {(r, c) for r in range(T) for c in range(r, T)}
+    units = [(rs, cs) for rs in itertools.combinations(range(T), 2) for cs in itertools.combinations(range(T), 2)]
+    best = None
+    for k in range(1, 4):
+        for combo in itertools.combinations(units, k):
+            cells = [(min(r, c), max(r, c)) for rs, cs in combo for r in rs for c in cs]
+            if need <= set(cells):
+                extra = len(cells) - len(need)
+                best = extra if best is None else min(best, extra)
+        if best is not None:
+            break
+    assert best == T // 2
+
+
+def _units_without_waste(T):
+    """Pair units whose four blocks serve four different block pairs {r, c}
+    (a block below the diagonal serving its mirror)."""
+    import itertools
+    out = set()
+    for rs in itertools.combinations(range(T), 2):
+        for cs in itertools.combinations(range(T), 2):
+            keys = frozenset((min(r, c), max(r, c)) for r in rs for c in cs)
+            if len(keys) == 4:
+                out.add(keys)
+    return sorted(tuple(sorted(u)) for u in out)
+
+
+def _exact_cover_exists(T):
+    """Whether units without waste can cover every block pair of a T x T
+    symmetric output exactly once (Knuth's Algorithm X, columns as sets)."""
+    units = _units_without_waste(T)
+    cols = {(r, c): set() for r in range(T) for c in range(r, T)}
+    for i, u in enumerate(units):
+        for k in u:
+            cols[k].add(i)
+
+    def search():
+        if not cols:
+            return True
+        key = min(cols, key=lambda k: len(cols[k]))
+        for i in sorted(cols[key]):
+            removed = []
+            for k in units[i]:
+                for j in cols[k]:
+                    for k2 in units[j]:
+                        if k2 != k:
+                            cols[k2].discard(j)
+                removed.append((k, cols.pop(k)))
+            if search():
+                return True
+            for k, rows in reversed(removed):
+                cols[k] = rows
+                for j in rows:
+                    for k2 in units[j]:
+                        if k2 != k:
+                            cols[k2].add(j)
+        return False
+
+    return search()
+
+
+def test_the_parity_bound_not_the_count_decides_even_with_mirrors():
+    # T = 8: 36 block pairs would fit 9 units exactly by count, but every index
+    # has an odd number (7) of off-diagonal pairs, so no cover without waste
+    # exists; T = 7 (even counts) has one, which shows the search finds covers
+    assert not _exact_cover_exists(8)
+    assert _exact_cover_exists(7)
