@@ -137,7 +137,9 @@ def dense_step(params: Sequence, grads: Sequence, momenta: Sequence, shapes: Seq
                 u = torch.empty_like(grads[j])
                 ops.momentum(grads[j], momenta[j], u)
                 upd[j] = u
-            if world == 1:
+            if not distributed:
+                # no process group: this process owns every matrix (an initialised
+                # group, even of one rank, goes through the exchange below)
                 full = torch.stack([upd[j] for j in members])
                 ops.ns(full)
                 for k, j in enumerate(members):

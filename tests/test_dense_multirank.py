@@ -85,7 +85,7 @@ def _worker(rank, world, port, out):
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 3, 4])
+@pytest.mark.parametrize("world", [1, 2, 3, 4])
 def test_dense_step_matches_the_full_matrices(world):
     port = _free_port()
     with mp.Manager() as mgr:

@@ -5,8 +5,10 @@ batched Newton-Schulz call per shape between the momentum and update calls.
 Its result must match the fp64 oracle (momentum bit for bit, the
 orthogonalised update within 2e-2), and equal, bit for bit, the fused step on
 the same matrices given the same fp32 shape scale (the dense path hands the
-full matrix's scale to the update as an fp32 argument).  The all-to-all of
-more ranks is covered on CPU by tests/test_dense_multirank.py.
+full matrix's scale to the update as an fp32 argument).  With an initialised
+one-rank NCCL group the same step runs through the exchange (both
+all_to_all_single calls on CUDA tensors) and must give the same bits.  The
+all-to-all of more ranks is covered on CPU by tests/test_dense_multirank.py.
 """
 
 import numpy as np
@@ -76,3 +78,37 @@ def test_single_rank_dense_step_matches_oracle(mk):
         err = rel_fro(-np32(p2), ref["O"][0])
         print(f"dense matrix {j} {r}x{c}: rel {err:.3e}")
         assert err < 2e-2, (j, err)
+
+
+def test_exchange_over_a_one_rank_nccl_group_equals_the_local_path(mk):
+    # An initialised process group, even of one rank, sends the update through
+    # the exchange: both all_to_all_single calls run on NCCL with CUDA tensors
+    # and the library's kernels on the owner, on a side stream.  One rank owns
+    # everything, so the result must equal the path without a group bit for bit.
+    import socket
+
+    import torch.distributed as dist
+    if not dist.is_nccl_available():
+        pytest.skip("NCCL backend not available")
+    mats = _inputs(4300)
+    p_ref = [W.clone() for W, _, _ in mats]
+    m_ref = [m.clone() for _, _, m in mats]
+    dense.dense_step(p_ref, [g for _, g, _ in mats], m_ref, SHAPES)
+    with socket.socket() as s_:
+        s_.bind(("127.0.0.1", 0))
+        port = s_.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        params = [W.clone() for W, _, _ in mats]
+        moms = [m.clone() for _, _, m in mats]
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        dense.dense_step(params, [g for _, g, _ in mats], moms, SHAPES, stream=side)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    assert mk.muon_get_device_status() == 0
+    for j in range(len(SHAPES)):
+        assert np.array_equal(bits16(params[j]), bits16(p_ref[j])), j
+        assert np.array_equal(bits32(moms[j]), bits32(m_ref[j])), j
