@@ -24,13 +24,16 @@
 // below the largest entry.  The powers of two fold into the epilogues'
 // existing constants, exactly.
 // X is carried between iterations as a pair of halves, hi (bf16(X) or
-// fp16(sigma X)) and lo = bf16(sigma X - hi): the tensor cores read hi only,
-// while the a X term of the epilogue uses hi + lo.  Rounding X itself to 16
-// bits would inject noise into every singular direction each iteration, and
-// the quintic multiplies small singular values by up to a = 3.4445 per step,
-// so on rank-deficient or ill-conditioned inputs that noise grows to percent
-// level in the output (10% with bf16, 1-2% with fp16); with the lo half it
-// stays near 2^-17.
+// fp16(sigma X)) and lo, the remainder X - hi in 8 bits (e5m2 times a power
+// of two S chosen from the same bound): the tensor cores read hi only, while
+// the a X term of the epilogue uses hi + lo.  Rounding X itself to 16 bits
+// would inject noise into every singular direction each iteration, and the
+// quintic multiplies small singular values by up to a = 3.4445 per step, so
+// on rank-deficient or ill-conditioned inputs that noise grows to percent
+// level in the output (10% with bf16, 1-2% with fp16).  The remainder is at
+// most hi's rounding unit, so its 8 bits leave about 2^-11 of |X| per entry;
+// the last iteration's input, whose rounding passes through one step only,
+// carries no lo.
 //
 // Design: persistent CTA pairs (clusters of 2), one CTA per SM, 320 threads,
 // warp-specialised.  A pair computes a 256 x 256 output tile with
@@ -41,9 +44,9 @@
 // shared memory, which is what keeps its bandwidth below the tensor cores'
 // appetite.
 //   warp 0 lane 0  TMA producer (both CTAs): 128x64 bf16 boxes, 128-byte
-//                  swizzle, a ring of stages of one or two k-blocks
-//                  (Layout); completion is signalled on the even CTA's
-//                  "full" barrier, which counts the bytes of both halves;
+//                  swizzle, a ring of stages of two k-blocks (Layout); each
+//                  k-block completes on its own "full" barrier in the even
+//                  CTA, which counts the bytes of both halves;
 //   warp 1         TMEM allocation of 512 columns (two 128 x 256 fp32
 //                  accumulators) in both CTAs; lane 0 of the even CTA issues
 //                  the MMAs and multicasts tcgen05.commit to both CTAs;
