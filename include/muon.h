@@ -240,14 +240,14 @@ int muon_step_batched_after(void *param, const void *grad, float *momentum, int6
  * the GPU).  param_host (bf16, in/out), grad_host (bf16) and momentum_host
  * (fp32, in/out) are page-locked host arrays (cudaHostAlloc /
  * cudaHostRegister) of batch matrices rows x cols.  The batch is streamed
- * through the GPU `chunk` matrices at a time (0: 8) in two device slots:
+ * through the GPU `chunk` matrices at a time (0: 8) in three device slots:
  * copies in and out run on two internal streams and overlap the compute of
  * the neighbouring chunk, which runs on `stream` and is muon_step_batched
  * (bit for bit muon_momentum_update -> muon_ns_batched ->
  * muon_apply_update).  The call returns once the work is enqueued; when
  * `stream` reaches it, the host arrays hold the updated parameters and
  * momentum (do not touch them before).
- * Device memory (2 slots of 12 bytes per element plus one step workspace
+ * Device memory (3 slots of 12 bytes per element plus one step workspace
  * of `chunk` matrices) is allocated and freed stream-ordered on
  * `stream`.  Errors: MUON_ERR_INVALID_ARG for bad sizes or null pointers,
  * MUON_ERR_UNSUPPORTED for rows or cols not multiples of 8 or pageable host

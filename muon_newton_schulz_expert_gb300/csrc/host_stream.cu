@@ -8,16 +8,21 @@
 // offloaded cut the optimizer step from 41.7 s to 2.2 s.
 //
 // Design: the batch is cut into chunks of `chunk` matrices that rotate through
-// two device slots.  For chunk k (slot k % 2):
-//   copy-in stream   waits until slot k%2's previous chunk has been copied out,
+// three device slots.  For chunk k (slot k % 3):
+//   copy-in stream   waits until the slot's previous chunk has been copied out,
 //                    then copies gradients, momentum and parameters in;
 //   caller's stream  waits for the copy-in, runs the fused step (momentum ->
 //                    Newton-Schulz -> update, muon_step_batched) on the slot;
 //   copy-out stream  waits for the compute, copies parameters and momentum out.
 // Copies of chunk k+1 and k-1 therefore overlap the compute of chunk k.  The
+// host link, not the compute, bounds the call, so the copy-in stream must
+// never wait: with two slots it waited for chunk k-2's copy-out before chunk
+// k's copy-in, idling the link once per two chunks; a third slot gives the
+// copy-out a chunk's time of slack (3.5-5.6% faster, back to back; the link's
+// speed drifts between runs on a shared host).  The
 // caller's stream finally waits for the last copy-out, so completion of the
 // call on that stream means the host arrays hold the result.  Device memory
-// (two slots and one Newton-Schulz workspace) is allocated and freed
+// (three slots and one Newton-Schulz workspace) is allocated and freed
 // stream-ordered on the caller's stream.
 #include <algorithm>
 
@@ -38,17 +43,20 @@ bool is_host_accessible_pinned(const void *p) {
 // The side streams and every event the call records, all created before any
 // device memory is allocated, so that no failure after the allocation can
 // skip the join of the side streams or the stream-ordered free.
+constexpr int kSlots = 3;   // device slots the chunks rotate through
+
 struct Streams {
   cudaStream_t in = nullptr, out = nullptr;
-  cudaEvent_t in_done[2] = {}, compute_done[2] = {}, out_done[2] = {};
+  cudaEvent_t in_done[kSlots] = {}, compute_done[kSlots] = {}, out_done[kSlots] = {};
   cudaEvent_t ready = nullptr, tail[2] = {};
   ~Streams() {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSlots; ++i) {
       if (in_done[i]) cudaEventDestroy(in_done[i]);
       if (compute_done[i]) cudaEventDestroy(compute_done[i]);
       if (out_done[i]) cudaEventDestroy(out_done[i]);
-      if (tail[i]) cudaEventDestroy(tail[i]);
     }
+    for (int i = 0; i < 2; ++i)
+      if (tail[i]) cudaEventDestroy(tail[i]);
     if (ready) cudaEventDestroy(ready);
     if (in) cudaStreamDestroy(in);    // deferred by CUDA until the enqueued work is done
     if (out) cudaStreamDestroy(out);
@@ -57,12 +65,13 @@ struct Streams {
     if (cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking) != cudaSuccess) return false;
     if (cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking) != cudaSuccess) return false;
     if (cudaEventCreateWithFlags(&ready, cudaEventDisableTiming) != cudaSuccess) return false;
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < kSlots; ++i)
       if (cudaEventCreateWithFlags(&in_done[i], cudaEventDisableTiming) != cudaSuccess ||
           cudaEventCreateWithFlags(&compute_done[i], cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&out_done[i], cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&tail[i], cudaEventDisableTiming) != cudaSuccess)
+          cudaEventCreateWithFlags(&out_done[i], cudaEventDisableTiming) != cudaSuccess)
         return false;
+    for (int i = 0; i < 2; ++i)
+      if (cudaEventCreateWithFlags(&tail[i], cudaEventDisableTiming) != cudaSuccess) return false;
     return true;
   }
 };
@@ -98,7 +107,7 @@ extern "C" int muon_step_host(void *param_host, const void *grad_host, float *mo
     return MUON_ERR_CUDA;
   }
   uint8_t *dev = nullptr;
-  if (alloc_async(reinterpret_cast<void **>(&dev), 2 * slot_bytes + ws, s) != cudaSuccess || !dev) {
+  if (alloc_async(reinterpret_cast<void **>(&dev), kSlots * slot_bytes + ws, s) != cudaSuccess || !dev) {
     cudaGetLastError();
     return MUON_ERR_NO_MEMORY;
   }
@@ -111,9 +120,9 @@ extern "C" int muon_step_host(void *param_host, const void *grad_host, float *mo
   auto *ph = static_cast<uint8_t *>(param_host);
   auto *gh = static_cast<const uint8_t *>(grad_host);
   auto *mh = reinterpret_cast<uint8_t *>(momentum_host);
-  bool used[2] = {false, false};
+  bool used[kSlots] = {};
   for (int64_t b0 = 0, k = 0; b0 < batch && status == MUON_OK; b0 += ch, ++k) {
-    const int slot = (int)(k & 1);
+    const int slot = (int)(k % kSlots);
     const int64_t nb = std::min(ch, batch - b0);
     uint8_t *base = dev + slot * slot_bytes;
     auto *g_d = base, *p_d = base + g_bytes;
@@ -132,7 +141,7 @@ extern "C" int muon_step_host(void *param_host, const void *grad_host, float *mo
     // compute on the caller's stream
     cudaStreamWaitEvent(s, st.in_done[slot], 0);
     status = muon_step_batched(p_d, g_d, m_d, nb, rows, cols, mu, nesterov, steps, coeffs, eps, lr, weight_decay,
-                               scale, dev + 2 * slot_bytes, ws, stream);
+                               scale, dev + kSlots * slot_bytes, ws, stream);
     if (status != MUON_OK) break;
     cudaEventRecord(st.compute_done[slot], s);
     // copy out
