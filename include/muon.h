@@ -257,6 +257,28 @@ int muon_step_host(void *param_host, const void *grad_host, float *momentum_host
                    int64_t cols, float mu, int nesterov, int steps, const float coeffs[3], float eps, float lr,
                    float weight_decay, float scale, int64_t chunk, muon_stream_t stream);
 
+/* muon_step_host over several groups of matrices (each group one shape, its
+ * own page-locked arrays and shape scale) in one pipeline: the chunks of all
+ * groups, in order, rotate through the same device slots, so the host link
+ * does not drain between groups as it does between separate calls (a model's
+ * expert matrices come in several shapes).  Each group's result is bit for
+ * bit that of muon_step_host on it.  Slots and workspace are sized for the
+ * largest group shape.  A group with batch 0 is skipped.  Errors as
+ * muon_step_host, checked for every group before any CUDA call, and
+ * MUON_ERR_INVALID_ARG for ngroups < 0 or groups == NULL with ngroups > 0.
+ */
+typedef struct {
+  void *param_host;          /* bf16, in/out */
+  const void *grad_host;     /* bf16 */
+  float *momentum_host;      /* fp32, in/out */
+  int64_t batch, rows, cols;
+  float scale;               /* <= 0: the default scale of rows x cols */
+} muon_host_group;
+
+int muon_step_host_grouped(const muon_host_group *groups, int ngroups, float mu, int nesterov, int steps,
+                           const float coeffs[3], float eps, float lr, float weight_decay, int64_t chunk,
+                           muon_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * AdamW for the parameters Muon does not take (FlexShard section: routers and
  * embeddings use AdamW, with two fp32 states per parameter).  Reading taken:

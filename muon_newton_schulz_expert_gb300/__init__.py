@@ -45,6 +45,13 @@ class TraceEntry(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_char_p), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
 
 
+class HostGroup(ctypes.Structure):
+    """muon_host_group: one shape group of page-locked host arrays."""
+    _fields_ = [("param_host", ctypes.c_void_p), ("grad_host", ctypes.c_void_p), ("momentum_host", ctypes.c_void_p),
+                ("batch", ctypes.c_int64), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("scale", ctypes.c_float)]
+
+
 SIGNATURES = {
     "muon_momentum_update": (_INT, [_P, _P, _P, _I64, _F, _INT, _P]),
     "muon_momentum_update_f32": (_INT, [_P, _P, _P, _I64, _F, _INT, _P]),
@@ -66,6 +73,7 @@ SIGNATURES = {
     "muon_step_batched_after": (_INT, [_P, _P, _P, _I64, _I64, _I64, _F, _INT, _INT, _P, _F, _F, _F, _F, _P, _SIZE,
                                        _P, _P]),
     "muon_step_host": (_INT, [_P, _P, _P, _I64, _I64, _I64, _F, _INT, _INT, _P, _F, _F, _F, _F, _I64, _P]),
+    "muon_step_host_grouped": (_INT, [_P, _INT, _F, _INT, _INT, _P, _F, _F, _F, _I64, _P]),
     "muon_adamw_update": (_INT, [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P]),
     "muon_adamw_update_f32": (_INT, [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P]),
     "muon_get_device_status": (_INT, [_P]),
@@ -362,23 +370,41 @@ def muon_step_batched_schedule(param, grad, momentum, coeff_rows, *, mu=0.95, ne
         float(lr), float(weight_decay), float(scale), ws, ws_bytes, _stream_handle(stream)))
 
 
-def muon_step_host(param_host, grad_host, momentum_host, *, mu=0.95, nesterov=True, steps=5, coeffs=QUINTIC,
-                   eps=1e-7, lr=0.02, weight_decay=0.1, scale=0.0, chunk=0, stream=None):
-    """One Muon step on pinned host tensors (batch, rows, cols), streamed through the GPU."""
+def _host_arrays(param_host, grad_host, momentum_host):
     import torch
     for t, n, dt in ((param_host, "param_host", torch.bfloat16), (grad_host, "grad_host", torch.bfloat16),
                      (momentum_host, "momentum_host", torch.float32)):
         if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != dt or not t.is_contiguous():
             raise TypeError(f"{n} must be a contiguous host {dt} tensor")
-        if not t.is_pinned():
+        if t.numel() and not t.is_pinned():
             raise ValueError(f"{n} must be in page-locked (pinned) host memory")
     if not (param_host.shape == grad_host.shape == momentum_host.shape):
         raise ValueError("param, grad and momentum must have the same shape")
-    b, r, c = _bmn(param_host)
+    return _bmn(param_host)
+
+
+def muon_step_host(param_host, grad_host, momentum_host, *, mu=0.95, nesterov=True, steps=5, coeffs=QUINTIC,
+                   eps=1e-7, lr=0.02, weight_decay=0.1, scale=0.0, chunk=0, stream=None):
+    """One Muon step on pinned host tensors (batch, rows, cols), streamed through the GPU."""
+    b, r, c = _host_arrays(param_host, grad_host, momentum_host)
     _check("muon_step_host", lib().muon_step_host(
         _ptr(param_host), _ptr(grad_host), _ptr(momentum_host), b, r, c, float(mu), int(bool(nesterov)), int(steps),
         _coeffs(coeffs), float(eps), float(lr), float(weight_decay), float(scale), int(chunk),
         _stream_handle(stream)))
+
+
+def muon_step_host_grouped(groups, *, mu=0.95, nesterov=True, steps=5, coeffs=QUINTIC, eps=1e-7, lr=0.02,
+                           weight_decay=0.1, chunk=0, stream=None):
+    """muon_step_host over several shape groups in one pipeline.  groups: a list of
+    (param_host, grad_host, momentum_host) or (param_host, grad_host, momentum_host, scale)."""
+    arr = (HostGroup * max(1, len(groups)))()
+    for i, grp in enumerate(groups):
+        p, g, m = grp[:3]
+        b, r, c = _host_arrays(p, g, m)
+        arr[i] = HostGroup(p.data_ptr(), g.data_ptr(), m.data_ptr(), b, r, c, float(grp[3]) if len(grp) > 3 else 0.0)
+    _check("muon_step_host_grouped", lib().muon_step_host_grouped(
+        ctypes.cast(arr, ctypes.c_void_p), len(groups), float(mu), int(bool(nesterov)), int(steps), _coeffs(coeffs),
+        float(eps), float(lr), float(weight_decay), int(chunk), _stream_handle(stream)))
 
 
 def muon_default_scale(rows, cols):

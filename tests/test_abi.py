@@ -218,3 +218,22 @@ def test_allocation_failure_injection_counts_on_the_host(lib):
     assert lib.muon_inject_alloc_failures(0) == 2
     assert lib.muon_inject_alloc_failures(-1) == -1        # MUON_ERR_INVALID_ARG
     assert lib.muon_inject_alloc_failures(0) == 0
+
+
+def test_grouped_host_step_rejects_bad_groups_on_the_host(lib):
+    import muon_newton_schulz_expert_gb300 as m
+    co = (ctypes.c_float * 3)(3.4445, -4.7750, 2.0315)
+    f = lib.muon_step_host_grouped
+    assert f(None, 0, 0.95, 1, 5, co, 1e-7, 0.02, 0.1, 0, None) == 0        # nothing to do
+    assert f(None, -1, 0.95, 1, 5, co, 1e-7, 0.02, 0.1, 0, None) == -1
+    assert f(None, 2, 0.95, 1, 5, co, 1e-7, 0.02, 0.1, 0, None) == -1
+    buf = ctypes.create_string_buffer(1024)
+    ptr = ctypes.addressof(buf)
+    groups = (m.HostGroup * 2)(m.HostGroup(ptr, ptr, ptr, 0, 64, 64, 0.0), m.HostGroup(ptr, ptr, ptr, 2, 64, 60, 0.0))
+    g = ctypes.cast(groups, ctypes.c_void_p)
+    assert f(g, 2, 0.95, 1, 5, co, 1e-7, 0.02, 0.1, 0, None) == -2         # cols not a multiple of 8
+    groups[1] = m.HostGroup(None, ptr, ptr, 2, 64, 64, 0.0)
+    assert f(g, 2, 0.95, 1, 5, co, 1e-7, 0.02, 0.1, 0, None) == -1         # null parameter array
+    groups[1] = m.HostGroup(ptr, ptr, ptr, -1, 64, 64, 0.0)
+    assert f(g, 2, 0.95, 1, 5, co, 1e-7, 0.02, 0.1, 0, None) == -1         # negative batch
+    assert f(g, 2, 0.95, 1, 5, co, 1e-7, 0.02, 0.1, -1, None) == -1        # negative chunk

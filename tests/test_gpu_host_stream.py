@@ -53,3 +53,27 @@ def test_host_streamed_step_rejects_pageable_memory(mk):
     W = torch.zeros(2, 64, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         mk.muon_step_host(W, W, torch.zeros(2, 64, 64))
+
+
+def test_grouped_host_step_equals_one_call_per_group(mk):
+    # one pipeline over three shapes (and an empty group) gives each group the
+    # bits of its own muon_step_host call; chunk 4 makes the slots rotate
+    # across group boundaries mid-cycle
+    shapes = [(11, 256, 768), (0, 64, 64), (5, 640, 192), (3, 128, 128)]
+    groups, singles = [], []
+    for i, (b, r, c) in enumerate(shapes):
+        g = workloads.gradients(max(b, 1), r, c, 720 + i, device="cpu")[:b].contiguous()
+        W = workloads.parameters(max(b, 1), r, c, 730 + i, device="cpu")[:b].contiguous()
+        m = (torch.randn(max(b, 1), r, c, generator=torch.Generator().manual_seed(740 + i)) * 0.1)[:b].contiguous()
+        scale = 0.5 if i == 2 else 0.0
+        groups.append((W.pin_memory(), g.pin_memory(), m.pin_memory(), scale))
+        singles.append((W.clone().pin_memory(), g.pin_memory(), m.clone().pin_memory(), scale))
+    mk.muon_step_host_grouped(groups, chunk=4)
+    for W, g, m, scale in singles:
+        if W.shape[0]:
+            mk.muon_step_host(W, g, m, chunk=4, scale=scale)
+    torch.cuda.synchronize()
+    assert mk.muon_get_device_status() == 0
+    for (Wg, _, mg, _), (Ws, _, ms, _) in zip(groups, singles):
+        assert torch.equal(Wg.view(torch.int16), Ws.view(torch.int16))
+        assert torch.equal(mg, ms)
