@@ -264,8 +264,9 @@ int muon_step_host(void *param_host, const void *grad_host, float *momentum_host
  * expert matrices come in several shapes).  Each group's result is bit for
  * bit that of muon_step_host on it.  Slots and workspace are sized for the
  * largest group shape.  A group with batch 0 is skipped.  Errors as
- * muon_step_host, checked for every group before any CUDA call, and
- * MUON_ERR_INVALID_ARG for ngroups < 0 or groups == NULL with ngroups > 0.
+ * muon_step_host, checked for every group before anything is allocated or
+ * enqueued, and MUON_ERR_INVALID_ARG for ngroups < 0 or groups == NULL with
+ * ngroups > 0.
  */
 typedef struct {
   void *param_host;          /* bf16, in/out */
