@@ -2,8 +2,11 @@
 
 Each translation unit is compiled by its own nvcc process in parallel, then
 linked into ``_lib/libmuon.so`` next to this file with the CUDA runtime linked
-statically.  A rebuild is skipped when the library is newer than every source
-and header.
+statically.  ``build(checked=True)`` makes ``_lib/libmuon_checked.so`` from the
+same sources with ``-DMUON_DEVICE_CHECKS``: the kernels then test, before each
+access that would fault if it broke, the invariants they rely on, and report a
+broken one as MUON_ERR_DEVICE instead of making the access.  A rebuild is
+skipped when the library is newer than every source and header.
 """
 
 from __future__ import annotations
@@ -20,6 +23,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmuon.so")
+LIB_CHECKED = os.path.join(OUT_DIR, "libmuon_checked.so")
 SOURCES = ["api.cu", "elementwise.cu", "gemm_tc.cu", "gemm_f32.cu", "ns_static.cu", "host_stream.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
@@ -40,21 +44,25 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(checked: bool = False) -> bool:
+    lib = LIB_CHECKED if checked else LIB
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Build libmuon.so if needed and return its path."""
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Build libmuon.so (or, checked, libmuon_checked.so) if needed and return its path."""
+    lib = LIB_CHECKED if checked else LIB
+    if not force and up_to_date(checked):
+        return lib
     nvcc = _nvcc()
-    obj_dir = os.path.join(OUT_DIR, "obj")
+    obj_dir = os.path.join(OUT_DIR, "obj_checked" if checked else "obj")
     os.makedirs(obj_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose else []
+    if checked:
+        extra.append("-DMUON_DEVICE_CHECKS")
 
     def compile_one(src):
         obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
@@ -68,14 +76,23 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_all(force: bool = False) -> list[str]:
+    """Both libraries, their translation units compiled side by side."""
+    with concurrent.futures.ThreadPoolExecutor(max_workers=2) as ex:
+        return list(ex.map(lambda c: build(force=force, checked=c), (False, True)))
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    if "--all" in sys.argv:
+        print(build_all(force="--force" in sys.argv))
+    else:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked="--checked" in sys.argv))

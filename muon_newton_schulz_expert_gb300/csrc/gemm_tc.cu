@@ -310,8 +310,26 @@ __device__ __forceinline__ bool wait_polled(uint32_t bar, uint32_t parity, Watch
   }
 }
 
+// Checked builds (-DMUON_DEVICE_CHECKS: the library's variant libmuon_checked.so)
+// test, before each access that would fault if it broke, an invariant the
+// kernels hold by construction: a TMA coordinate's x on a 16-element boundary
+// (16 bytes or more), no store at a negative coordinate, a shared-memory
+// offset inside its slot, a TMEM column inside the allocation.  A broken one
+// sets MUON_ERR_DEVICE in the error word and the access is skipped (a skipped
+// load leaves its barrier short, so the wait for it times out and the kernel
+// returns).  The normal build compiles the checks away.
+#ifdef MUON_DEVICE_CHECKS
+__device__ __forceinline__ bool dcheck(bool ok, unsigned *err) {
+  if (!ok && err) atomicOr(err, kErrDevice);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool dcheck(bool, unsigned *) { return true; }
+#endif
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
-                                            int c2) {
+                                            int c2, unsigned *err) {
+  if (!dcheck((c0 & 15) == 0 && c2 >= 0, err)) return;
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
           dst),
@@ -322,7 +340,8 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 // Pair form: the completion is signalled on an mbarrier that may live in the
 // peer CTA (a shared::cluster address), here always the pair's even CTA.
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
-                                                 int c2) {
+                                                 int c2, unsigned *err) {
+  if (!dcheck((c0 & 15) == 0 && c2 >= 0, err)) return;
   asm volatile(
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
       "[%2];" ::"r"(dst),
@@ -356,7 +375,9 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2) {
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2,
+                                             unsigned *err) {
+  if (!dcheck((c0 & 15) == 0 && c0 >= 0 && c1 >= 0 && c2 >= 0, err)) return;
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(src), "r"(c0), "r"(c1), "r"(c2)
@@ -656,18 +677,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             // K-major operands: one box of 128 rows x 64 K-columns.  MN-major
             // operands: boxes of 64 M/N-columns x 64 K-rows, one per swizzle atom.
             if (!A_MN) {
-              tma_load_3d_pair(sa, &tmA, full0, kb * BK, arow, mat);
+              tma_load_3d_pair(sa, &tmA, full0, kb * BK, arow, mat, p.err);
             } else {
 #pragma unroll
               for (int q = 0; q < BM / 64; ++q)
-                tma_load_3d_pair(sa + q * (64 * BK * 2), &tmA, full0, arow + q * 64, kb * BK, mat);
+                tma_load_3d_pair(sa + q * (64 * BK * 2), &tmA, full0, arow + q * 64, kb * BK, mat, p.err);
             }
             if (!B_MN) {
-              tma_load_3d_pair(sb, &tmB, full0, kb * BK, brow, mat);
+              tma_load_3d_pair(sb, &tmB, full0, kb * BK, brow, mat, p.err);
             } else {
 #pragma unroll
               for (int q = 0; q < BNH / 64; ++q)
-                tma_load_3d_pair(sb + q * (64 * BK * 2), &tmB, full0, brow + q * 64, kb * BK, mat);
+                tma_load_3d_pair(sb + q * (64 * BK * 2), &tmB, full0, brow + q * 64, kb * BK, mat, p.err);
             }
           }
           if (++stage == STAGES) {
@@ -766,6 +787,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int LOB = Layout<EPI>::lo_bytes;     // one 32 x CW box of the 8-bit low half
     constexpr int PIECES = CW / 8;                 // 16-byte pieces per 16-bit box row
     static_assert(APPLY || CW == 32, "aX + BX moves 32-column chunks");
+    // every lane's 16-byte accesses stay inside its slot's boxes, and every
+    // chunk's accumulator columns inside the TMEM allocation
+    static_assert(31 * (2 * CW) + (PIECES - 1) * 16 + 16 <= BOXB, "16-bit box rows stay inside the box");
+    static_assert(APPLY || 31 * 32 + 16 + 16 <= LOB, "low-half box rows stay inside the box");
+    static_assert(ACC_COLS + 128 + NCH * CW <= TMEM_COLS, "accumulator columns stay inside TMEM");
     const int ew = warp - 2;
     const int q = warp & 3, half = ew >> 2;
     uint8_t *ebase = epi_smem + ew * SLOTS * IN_BYTES;
@@ -778,9 +804,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t dst = ebase_s + slot * IN_BYTES, bar = EBAR(ew * SLOTS + slot);
       fence_proxy_async_smem();
       mbar_expect_tx(bar, etx);
-      tma_load_3d(dst, &p.tm_src, bar, col0_, row0_, m_);
-      if (lo_in) tma_load_3d(dst + BOXB, &p.tm_src_lo, bar, col0_, row0_, m_);
-      if (APPLY) tma_load_3d(dst + BOXB, &p.tm_out, bar, col0_, row0_, m_);  // W, stored over later
+      tma_load_3d(dst, &p.tm_src, bar, col0_, row0_, m_, p.err);
+      if (lo_in) tma_load_3d(dst + BOXB, &p.tm_src_lo, bar, col0_, row0_, m_, p.err);
+      if (APPLY) tma_load_3d(dst + BOXB, &p.tm_out, bar, col0_, row0_, m_, p.err);  // W, stored over later
       pending |= 1u << slot;
     };
     const int rbase = (int)rank * BM + q * 32;  // this warp's rows within a pair tile
@@ -883,8 +909,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_3d(&p.tm_out, ebuf_s, col0, row0, mat);
-          if (lo_out) tma_store_3d(&p.tm_out_lo, ebuf_s + BOXB, col0, row0, mat);
+          tma_store_3d(&p.tm_out, ebuf_s, col0, row0, mat, p.err);
+          if (lo_out) tma_store_3d(&p.tm_out_lo, ebuf_s + BOXB, col0, row0, mat, p.err);
           bulk_commit();
           bulk_wait_read_all();  // the stores have read the slot the next load fills
           // every lane has read this input slot: fetch chunk ch + SLOTS into it (possibly of the next tile)
@@ -925,6 +951,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     // (Reading it into registers for the whole tile before the accumulator is
     // ready measured 5% slower.)
     constexpr int SLOTS = Layout<EPI>::slots;
+    static_assert(31 * 64 + 3 * 16 + 16 <= EPI_BOX_BYTES, "direct box rows stay inside the box");
+    static_assert((31 * 32 + 31 + 1) * 2 <= EPI_BUF - EPI_BOX_BYTES, "mirror box entries stay inside the slot");
+    static_assert(ACC_COLS + 128 + CHUNKS * 32 <= TMEM_COLS, "accumulator columns stay inside TMEM");
     const int ew = warp - 2;
     const int q = warp & 3, half = ew >> 2;
     uint8_t *ebase = epi_smem + ew * SLOTS * EPI_BUF;   // slots of [direct box][mirror box]
@@ -939,7 +968,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t bar = EBAR(ew * SLOTS + slot);
       fence_proxy_async_smem();
       mbar_expect_tx(bar, EPI_BOX_BYTES);
-      tma_load_3d(ebase_s + slot * EPI_BUF, &p.tm_src, bar, col0_, row0_, m_);
+      tma_load_3d(ebase_s + slot * EPI_BUF, &p.tm_src, bar, col0_, row0_, m_, p.err);
       pending |= 1u << slot;
     };
     int acc = 0;
@@ -1024,8 +1053,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             if (lane == 0) {
               const uint32_t src = ebase_s + slot * EPI_BUF;
-              tma_store_3d(&p.tm_out, src, col0, row0, mat);
-              tma_store_3d(&p.tm_out_t, src + EPI_BOX_BYTES, row0, col0, mat);
+              tma_store_3d(&p.tm_out, src, col0, row0, mat, p.err);
+              tma_store_3d(&p.tm_out_t, src + EPI_BOX_BYTES, row0, col0, mat, p.err);
               bulk_commit();
             }
           } else {

@@ -237,3 +237,12 @@ def test_grouped_host_step_rejects_bad_groups_on_the_host(lib):
     groups[1] = m.HostGroup(ptr, ptr, ptr, -1, 64, 64, 0.0)
     assert f(g, 2, 0.95, 1, 5, co, 1e-7, 0.02, 0.1, 0, None) == -1         # negative batch
     assert f(g, 2, 0.95, 1, 5, co, 1e-7, 0.02, 0.1, -1, None) == -1        # negative chunk
+
+
+def test_checked_variant_builds_and_exports_every_symbol():
+    # the same sources with -DMUON_DEVICE_CHECKS (its GPU behaviour is checked
+    # in tests/test_gpu_checked_build.py)
+    path = mkbuild.build(checked=True)
+    raw = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(raw, n), n
