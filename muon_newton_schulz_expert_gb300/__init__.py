@@ -17,7 +17,10 @@ import ctypes
 import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_lib", "libmuon.so")
+# MUON_CHECKED=1 loads the checked build (device-side checks of the kernels'
+# TMA coordinates, reported as MUON_ERR_DEVICE), for example to run the tests on it
+CHECKED = os.environ.get("MUON_CHECKED") == "1"
+LIB_PATH = os.path.join(_PKG, "_lib", "libmuon_checked.so" if CHECKED else "libmuon.so")
 
 QUINTIC = (3.4445, -4.7750, 2.0315)
 

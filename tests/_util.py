@@ -28,7 +28,7 @@ def require_gpu():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import muon_newton_schulz_expert_gb300.build as b
-    b.build()
     import muon_newton_schulz_expert_gb300 as mk
+    b.build(checked=mk.CHECKED)
     mk.lib()
     return mk
